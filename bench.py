@@ -1,0 +1,350 @@
+"""Benchmark: one step = one forward + one backward pass of exact attention over
+one batch of synthetic bf16 input (every stage of the path: forward kernel,
+backward pre / main / post kernels), on the mid-length workload
+B=4, H=16, N=8192, d=128, non-causal (32k tokens, hidden 2048).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line. ``value`` is whole-job attention TFLOP/s (forward
+4*N^2*d per head plus backward 2.5x that), inputs resident in device memory;
+``e2e`` is the same metric through the public binding with host buffers, the
+host->device copies of q, k, v, dO and the device->host copies of o, lse, dq,
+dk, dv inside the timed region. ``--impl reference`` times the fp64 CPU oracle
+on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "mid"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_for(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "exact_attention_15_gb300", "csrc", rec["source"])
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    if sha != rec.get("source_sha256_16"):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ reference arm (oracle)
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from exact_attention_15_gb300 import workloads as W
+
+    w = W.WORKLOADS[WORKLOAD]
+    # bounded sample: one (batch, head) pair, every query row, forward + backward
+    inp = W.custom(1, 1, 1, w.N, w.N, w.d, w.scale, w.causal, seed=w.seed)
+    f64 = W.bf16_bits_to_f64
+    q, k, v, do = (f64(x[0, :, 0, :]) for x in (inp.q, inp.k, inp.v, inp.do))
+    flops = W.fwd_flops(1, 1, w.N, w.N, w.d, w.causal) * 3.5
+    for _ in range(args.warmup):
+        oracle.head_backward(q, k, v, do, w.scale, w.causal)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.head_backward(q, k, v, do, w.scale, w.causal)
+        times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    value = flops / sec / 1e12
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": "attention fwd+bwd TFLOP/s (bf16 inputs)", "value": value,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: B4 H16 N8192 d128 non-causal", "step_sample": "1 (batch, head) pair"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "one (batch, head) pair of the workload, all 8192 query rows, fwd+bwd, numpy fp64 BLAS"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_sample():
+    """The oracle on a bounded sample (one (b, h) pair), timed on the host."""
+    import oracle
+    from exact_attention_15_gb300 import workloads as W
+    w = W.WORKLOADS[WORKLOAD]
+    inp = W.custom(1, 1, 1, w.N, w.N, w.d, w.scale, w.causal, seed=w.seed)
+    f64 = W.bf16_bits_to_f64
+    q, k, v, do = (f64(x[0, :, 0, :]) for x in (inp.q, inp.k, inp.v, inp.do))
+    oracle.head_backward(q[:512], k, v, do[:512], w.scale, w.causal)  # warm BLAS
+    t0 = time.perf_counter()
+    oracle.head_backward(q, k, v, do, w.scale, w.causal)
+    sec = time.perf_counter() - t0
+    flops = W.fwd_flops(1, 1, w.N, w.N, w.d, w.causal) * 3.5
+    return {"value": flops / sec / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"one (batch, head) pair of the workload (8192x8192, d=128), fwd+bwd in {sec:.2f} s, numpy fp64 BLAS on all host cores"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import numpy as np
+    import torch
+    from exact_attention_15_gb300 import binding, workloads as W
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    binding.load()
+
+    w = W.WORKLOADS[WORKLOAD]
+    inp = W.generate(WORKLOAD)
+    dev = lambda bits: torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    q, k, v, do = dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.do)
+    B, H, N, d = w.B, w.H_q, w.N, w.d
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = binding.attn_bwd_workspace_bytes(B, H, H, N, N, d, 0, 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    def step():
+        st = binding.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              B, H, H, N, N, d, w.causal, None, w.scale, sp)
+        assert st == 0, st
+        st = binding.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                              B, H, H, N, N, d, w.causal, None, w.scale, 0, ws.data_ptr(), ws_bytes, sp)
+        assert st == 0, st
+
+    fwd_flops = W.fwd_flops(B, H, N, N, d, w.causal)
+    step_flops = fwd_flops * 3.5  # forward + 2.5x backward
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert binding.attn_check(sp) == 0
+
+    sampler = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    binding.attn_profile_enable(True)
+    binding.attn_profile_read()
+    sampler.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    binding.attn_profile_enable(False)
+    recs = binding.attn_profile_read()
+    ms_total = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms_total], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+        torch.distributed.barrier()
+    assert binding.attn_check(sp) == 0
+    ms_step = ms_total / args.steps
+    value = world * step_flops * args.steps / (ms_total * 1e-3) / 1e12
+
+    per_kernel = {}
+    for name, ms in recs:
+        per_kernel.setdefault(name, []).append(ms)
+    kt = {n: {"launches": len(v_), "avg_ms": sum(v_) / len(v_), "total_ms": sum(v_)} for n, v_ in per_kernel.items()}
+    tot = sum(x["total_ms"] for x in kt.values()) or 1.0
+    for x in kt.values():
+        x["share"] = x["total_ms"] / tot
+    peaks, peak_src = measured_peaks()
+    sustained = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    burst = float(peaks.get("bf16_tflops"))
+
+    def roof(kernel, flops_per_launch):
+        if kernel not in kt:
+            return None
+        ach = flops_per_launch / (kt[kernel]["avg_ms"] * 1e-3) / 1e12
+        tr = traffic_for(kernel)
+        return {"bound": "tensor", "achieved": ach, "peak": sustained, "unit": "TFLOP/s",
+                "frac": ach / sustained, "traffic": tr, "kernel": kernel,
+                "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+                "frac_of_burst": ach / burst, "frac_of_2250": ach / 2250.0}
+
+    dominant = max(kt, key=lambda n: kt[n]["total_ms"]) if kt else None
+    flops_of = {"attn_fwd_kernel": fwd_flops, "attn_bwd_main_kernel": 2.5 * fwd_flops}
+    roofline = roof(dominant, flops_of.get(dominant, 0.0)) if dominant in flops_of else None
+    roofline_fwd = roof("attn_fwd_kernel", fwd_flops)
+
+    # end to end through the public binding with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (inp.q, inp.k, inp.v, inp.do)]
+        ho = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+        hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        hdq, hdk, hdv = (torch.empty(t.shape, dtype=torch.bfloat16).pin_memory() for t in (q, k, v))
+        h2d = sum(t.numel() * t.element_size() for t in hq)
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+
+        def e2e_step():
+            for hsrc, ddst in zip(hq, (q, k, v, do)):
+                ddst.copy_(hsrc, non_blocking=True)
+            step()
+            for dsrc, hdst in ((o, ho), (lse, hl), (dq, hdq), (dk, hdk), (dv, hdv)):
+                hdst.copy_(dsrc, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = ev0.elapsed_time(ev1)
+        if world > 1:
+            t = torch.tensor([ms_e2e], device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": world * step_flops * args.steps / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": ms_e2e / args.steps}
+
+    if rank == 0:
+        cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline_sample()
+        fwd_ms = kt.get("attn_fwd_kernel", {}).get("avg_ms")
+        line = {
+            "metric": "attention fwd+bwd TFLOP/s (bf16, 1xGB300)", "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD}: B4 H16 N8192 d128 non-causal, scale 1/sqrt(128), fwd+bwd",
+                       "global_batch": B * world, "seq_len": N, "heads": H, "head_dim": d,
+                       "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (q, k, v, o, dO: 128 MiB each)"},
+            "fwd_tflops": (fwd_flops / (fwd_ms * 1e-3) / 1e12) if fwd_ms else None,
+            "kernels": kt,
+            "roofline": roofline,
+            "roofline_fwd": roofline_fwd,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": sum(x["launches"] for x in kt.values()),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,192 @@
+"""Thin Python binding over the C ABI in ``include/attn.h`` (ctypes).
+
+The functions named like the C entry points take raw device pointers (ints)
+and sizes exactly as the C functions do; ``forward`` / ``backward`` are
+convenience wrappers that take torch CUDA tensors, allocate the outputs (and
+the backward workspace) with torch, and pass pointers and torch's current
+stream. Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels. There is no fallback: if the library has not been
+built, or a call fails, an exception is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libattn_gb300.so")
+_lib = None
+
+ATTN_STATUS = {
+    0: "ATTN_OK", 1: "ATTN_ERR_NULL_PTR", 2: "ATTN_ERR_ALIGNMENT", 3: "ATTN_ERR_UNSUPPORTED_HEADDIM",
+    4: "ATTN_ERR_BAD_SHAPE", 5: "ATTN_ERR_GQA_RATIO", 6: "ATTN_ERR_CAUSAL_SHAPE",
+    7: "ATTN_ERR_WORKSPACE", 8: "ATTN_ERR_CUDA", 9: "ATTN_ERR_TIMEOUT", 10: "ATTN_ERR_NO_DEVICE",
+    11: "ATTN_ERR_UNSUPPORTED_DEVICE",
+}
+
+# name -> (restype, argtypes)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGS = {
+    "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, ctypes.c_float, _P]),
+    "attn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I, _I]),
+    "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
+                      ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
+    "attn_check": (_I, [_P]),
+    "attn_status_string": (ctypes.c_char_p, [_I]),
+    "attn_debug_exp2": (_I, [_P, _P, _I, _I, _P]),
+    "attn_set_wait_limit": (ctypes.c_longlong, [ctypes.c_longlong]),
+    "attn_profile_enable": (_I, [_I]),
+    "attn_profile_read": (_I, [_P, _I]),
+}
+
+KERNEL_NAMES = {1: "attn_fwd_kernel", 2: "attn_bwd_pre_kernel", 3: "attn_bwd_main_kernel",
+                4: "attn_bwd_post_kernel", 5: "exp2_probe_kernel"}
+
+
+class ProfileRecord(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int), ("ms", ctypes.c_float)]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {ATTN_STATUS.get(status, status)} ({status_string(status)})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Loads the shared library (once). Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(
+                f"CUDA library not built: {_LIB_PATH} is missing "
+                "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+# ------------------------------------------------------------------ raw C entry points
+
+def attn_fwd(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, causal, seqlens, scale, stream) -> int:
+    return load().attn_fwd(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, int(causal), seqlens,
+                           float(scale), stream)
+
+
+def attn_bwd_workspace_bytes(B, H_q, H_kv, N_q, N_k, d, varlen, deterministic) -> int:
+    return load().attn_bwd_workspace_bytes(B, H_q, H_kv, N_q, N_k, d, int(varlen), int(deterministic))
+
+
+def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H_q, H_kv, N_q, N_k, d, causal, seqlens,
+             scale, deterministic, workspace, workspace_bytes, stream) -> int:
+    return load().attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H_q, H_kv, N_q, N_k, d,
+                           int(causal), seqlens, float(scale), int(deterministic), workspace,
+                           workspace_bytes, stream)
+
+
+def attn_check(stream=None) -> int:
+    return load().attn_check(stream)
+
+
+def status_string(status: int) -> str:
+    return load().attn_status_string(int(status)).decode()
+
+
+attn_status_string = status_string
+
+
+def attn_debug_exp2(x, y, n, mode, stream) -> int:
+    return load().attn_debug_exp2(x, y, n, mode, stream)
+
+
+def attn_set_wait_limit(cycles: int) -> int:
+    return load().attn_set_wait_limit(int(cycles))
+
+
+def attn_profile_enable(enable: bool) -> int:
+    return load().attn_profile_enable(int(bool(enable)))
+
+
+def attn_profile_read(max_records: int = 65536):
+    """Returns [(kernel_name, ms), ...] for launches since the last read."""
+    buf = (ProfileRecord * max_records)()
+    n = load().attn_profile_read(ctypes.cast(buf, ctypes.c_void_p), max_records)
+    if n < 0:
+        raise AttnError(-n, "attn_profile_read")
+    return [(KERNEL_NAMES.get(buf[i].kernel, str(buf[i].kernel)), float(buf[i].ms)) for i in range(n)]
+
+
+# ------------------------------------------------------------------ torch convenience layer
+
+def _shape(q, k, cu_seqlens):
+    if cu_seqlens is not None:
+        T, H_q, d = q.shape
+        H_kv = k.shape[1]
+        return len(cu_seqlens) - 1, H_q, H_kv, T, k.shape[0], d
+    B, N_q, H_q, d = q.shape
+    return B, H_q, k.shape[2], N_q, k.shape[1], d
+
+
+def _stream_ptr():
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check(status, what):
+    if status != 0:
+        raise AttnError(status, what)
+
+
+def forward(q, k, v, scale=None, causal=False, cu_seqlens=None, out=None, lse=None):
+    """q [B, N_q, H_q, d] (or packed [T, H_q, d] with cu_seqlens), k/v likewise,
+    bf16 CUDA tensors. Returns (o, lse)."""
+    import torch
+    B, H_q, H_kv, N_q, N_k, d = _shape(q, k, cu_seqlens)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
+    o = out if out is not None else torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((H_q, N_q) if cu_seqlens is not None else (B, H_q, N_q),
+                          dtype=torch.float32, device=q.device)
+    cu_ptr = cu_seqlens.data_ptr() if cu_seqlens is not None else None
+    _check(attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                    B, H_q, H_kv, N_q, N_k, d, causal, cu_ptr, scale, _stream_ptr()), "attn_fwd")
+    return o, lse
+
+
+def backward(q, k, v, o, lse, dout, scale=None, causal=False, cu_seqlens=None,
+             deterministic=False, workspace=None):
+    """Returns (dq, dk, dv). The workspace is allocated with torch unless given."""
+    import torch
+    B, H_q, H_kv, N_q, N_k, d = _shape(q, k, cu_seqlens)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    nbytes = attn_bwd_workspace_bytes(B, H_q, H_kv, N_q, N_k, d, cu_seqlens is not None, deterministic)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    cu_ptr = cu_seqlens.data_ptr() if cu_seqlens is not None else None
+    _check(attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                    dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                    B, H_q, H_kv, N_q, N_k, d, causal, cu_ptr, scale, deterministic,
+                    workspace.data_ptr(), workspace.numel(), _stream_ptr()), "attn_bwd")
+    return dq, dk, dv

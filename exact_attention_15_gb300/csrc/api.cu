@@ -1,0 +1,418 @@
+// Host side of the C ABI declared in include/attn.h: argument validation,
+// tensor-memory-accelerator descriptors, launch plans and the device error word.
+// Order of work in every entry point: check arguments -> fill the parameter
+// block -> launch (the order the FlashAttention-1 code layout describes for its
+// C++ API: FlashAttention notes, xwysyy.cn, "code structure").
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/attn.h"
+#include "attn_common.cuh"
+
+namespace attn {
+cudaError_t launch_attn_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const FwdParams& p, dim3 grid,
+                            cudaStream_t stream);
+cudaError_t launch_exp2_probe(const float* x, float* y, int n, int mode, cudaStream_t stream);
+cudaError_t launch_attn_bwd(const BwdParams& p, const CUtensorMap* maps, cudaStream_t stream,
+                            long long rows_q, int n_sem, int n_work);
+}  // namespace attn
+
+using namespace attn;
+
+// One error word per device (each device gets its own copy of this variable).
+static __device__ int g_attn_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_err_ptr[kMaxDevices] = {};
+int g_dev_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 unsupported
+long long g_wait_limit = 2000000000ll;  // about one second of SM clock
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) return ATTN_ERR_NO_DEVICE;
+  if (*dev < 0 || *dev >= kMaxDevices) return ATTN_ERR_NO_DEVICE;
+  return ATTN_OK;
+}
+
+// Per-device set-up: capability check and the address of the error word.
+int device_setup(int dev, int** err_out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_dev_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return ATTN_ERR_NO_DEVICE;
+    if (major != 10 || minor != 3) {
+      g_dev_ok[dev] = -1;
+    } else {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_attn_error_word) != cudaSuccess) return ATTN_ERR_CUDA;
+      g_err_ptr[dev] = static_cast<int*>(ptr);
+      g_dev_ok[dev] = 1;
+    }
+  }
+  if (g_dev_ok[dev] < 0) return ATTN_ERR_UNSUPPORTED_DEVICE;
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return ATTN_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *err_out = g_err_ptr[dev];
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 4-D map over a [batch, rows, heads, d] bf16 tensor, one box = 128 rows x 64
+// columns of one head, 128-byte swizzle (so the tile lands in shared memory in
+// the layout the tcgen05 descriptors expect).
+int encode_rows_map(CUtensorMap* m, const void* base, int d, int heads, long long rows,
+                    long long batch) {
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(batch)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(d) * 2 * heads,
+                           static_cast<cuuint64_t>(d) * 2 * heads * rows};
+  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+struct Shape {
+  int B, H_q, H_kv, N_q, N_k, d;
+  bool varlen;
+  long long q_rows, k_rows;  // rows of the [rows, H, d] view (B*N fixed, T packed)
+  long long q_batch;         // TMA batch extent (B fixed, 1 packed)
+};
+
+int check_shape(int B, int H_q, int H_kv, int N_q, int N_k, int d, int causal,
+                const int* seqlens, Shape* s) {
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED_HEADDIM;
+  if (B < 0 || N_q < 0 || N_k < 0 || H_q <= 0 || H_kv <= 0) return ATTN_ERR_BAD_SHAPE;
+  if (H_q % H_kv != 0) return ATTN_ERR_GQA_RATIO;
+  if (H_q > 65535) return ATTN_ERR_BAD_SHAPE;
+  s->B = B; s->H_q = H_q; s->H_kv = H_kv; s->N_q = N_q; s->N_k = N_k; s->d = d;
+  s->varlen = seqlens != nullptr;
+  if (s->varlen) {
+    if (N_q != N_k) return ATTN_ERR_CAUSAL_SHAPE;  // one offset array for q and k/v
+    if (B < 1) return ATTN_ERR_BAD_SHAPE;
+    s->q_rows = N_q;
+    s->k_rows = N_k;
+    s->q_batch = 1;
+  } else {
+    if (causal && N_q != N_k) return ATTN_ERR_CAUSAL_SHAPE;
+    if (B > 65535) return ATTN_ERR_BAD_SHAPE;
+    s->q_rows = N_q;
+    s->k_rows = N_k;
+    s->q_batch = B;
+  }
+  // keep every element offset inside int64 and every TMA coordinate inside int32
+  const long long elems = static_cast<long long>(B) * (N_q + N_k) * H_q * d;
+  if (elems < 0 || elems > (1ll << 46)) return ATTN_ERR_BAD_SHAPE;
+  return ATTN_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// ---- kernel tracing: event pairs recorded around each launch
+struct ProfSlot {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfSlot> g_prof_open;   // recorded, not yet read
+std::vector<cudaEvent_t> g_prof_free;
+
+cudaEvent_t prof_event() {
+  if (!g_prof_free.empty()) {
+    cudaEvent_t e = g_prof_free.back();
+    g_prof_free.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Workspace plan of the backward pass.
+struct BwdPlan {
+  long long rows_q;     // rows of the [rows, H_q, d] view of q
+  long long slots;      // query-tile slots (deterministic semaphores), per head
+  long long n_work;     // CTAs of the main kernel (upper bound for packed inputs)
+  size_t acc_off, dvec_off, sem_off, total;
+};
+
+bool bwd_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d, bool varlen, bool det,
+              BwdPlan* pl) {
+  if (varlen) {
+    pl->rows_q = N_q;
+    pl->slots = (static_cast<long long>(N_q) + 127ll * B) / 128;
+    pl->n_work = (static_cast<long long>(N_k) + 127ll * B) / 128 * H_kv;
+  } else {
+    pl->rows_q = static_cast<long long>(B) * N_q;
+    pl->slots = static_cast<long long>(B) * ((N_q + 127) / 128);
+    pl->n_work = static_cast<long long>(B) * H_kv * ((N_k + 127) / 128);
+  }
+  if (pl->n_work > 0x7fffffffll || pl->slots * H_q > 0x7ffffffell) return false;
+  pl->acc_off = 0;
+  pl->dvec_off = align256(static_cast<size_t>(pl->rows_q) * H_q * d * 4);
+  pl->sem_off = pl->dvec_off + align256(static_cast<size_t>(pl->rows_q) * H_q * 4);
+  pl->total = pl->sem_off + (det ? align256(static_cast<size_t>(pl->slots * H_q + 1) * 4) : 0);
+  return true;
+}
+
+}  // namespace
+
+namespace attn {
+int prof_begin(int kernel, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (!g_prof_on) return -1;
+  ProfSlot s{kernel, prof_event(), prof_event()};
+  if (!s.start || !s.stop) return -1;
+  cudaEventRecord(s.start, stream);
+  g_prof_open.push_back(s);
+  return static_cast<int>(g_prof_open.size()) - 1;
+}
+void prof_end(int slot, cudaStream_t stream) {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (slot < static_cast<int>(g_prof_open.size())) cudaEventRecord(g_prof_open[slot].stop, stream);
+}
+}  // namespace attn
+
+extern "C" {
+
+int attn_profile_enable(int enable) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_on = enable != 0;
+  return ATTN_OK;
+}
+
+int attn_profile_read(attn_profile_record* out, int max_records) {
+  if (max_records > 0 && out == nullptr) return -ATTN_ERR_NULL_PTR;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  int n = 0;
+  for (const ProfSlot& s : g_prof_open) {
+    if (cudaEventSynchronize(s.stop) != cudaSuccess) return -ATTN_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, s.start, s.stop) != cudaSuccess) return -ATTN_ERR_CUDA;
+    if (n < max_records) out[n++] = attn_profile_record{s.kernel, ms};
+    g_prof_free.push_back(s.start);
+    g_prof_free.push_back(s.stop);
+  }
+  g_prof_open.clear();
+  return n;
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_NULL_PTR: return "null pointer";
+    case ATTN_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case ATTN_ERR_UNSUPPORTED_HEADDIM: return "unsupported head dimension (need 64 or 128)";
+    case ATTN_ERR_BAD_SHAPE: return "invalid size or scalar argument";
+    case ATTN_ERR_GQA_RATIO: return "H_q is not a multiple of H_kv";
+    case ATTN_ERR_CAUSAL_SHAPE: return "N_q != N_k where they must match";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device-side wait timed out";
+    case ATTN_ERR_NO_DEVICE: return "no usable CUDA device";
+    case ATTN_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103 (GB300 class)";
+    default: return "unknown status";
+  }
+}
+
+long long attn_set_wait_limit(long long cycles) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  const long long old = g_wait_limit;
+  if (cycles > 0) g_wait_limit = cycles;
+  return old;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
+             int H_kv, int N_q, int N_k, int d, int causal, const int* seqlens, float scale,
+             attn_stream_t stream) {
+  Shape s;
+  int st = check_shape(B, H_q, H_kv, N_q, N_k, d, causal, seqlens, &s);
+  if (st != ATTN_OK) return st;
+  // an empty tensor may come with a null pointer
+  const bool has_q = B > 0 && N_q > 0, has_k = B > 0 && N_k > 0;
+  if ((has_q && (!q || !o || !lse)) || (has_k && (!k || !v))) return ATTN_ERR_NULL_PTR;
+  if (!std::isfinite(scale)) return ATTN_ERR_BAD_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      (seqlens && (reinterpret_cast<uintptr_t>(seqlens) & 3u)))
+    return ATTN_ERR_ALIGNMENT;
+  if (B == 0 || N_q == 0) return ATTN_OK;
+  int dev;
+  if ((st = current_device(&dev)) != ATTN_OK) return st;
+  int* err = nullptr;
+  if ((st = device_setup(dev, &err)) != ATTN_OK) return st;
+
+  CUtensorMap tq, tk, tv;
+  // with no keys at all nothing is ever loaded from k/v; map q instead of an empty extent
+  const bool no_keys = (N_k == 0);
+  if (encode_rows_map(&tq, q, d, H_q, s.q_rows, s.q_batch) != ATTN_OK ||
+      encode_rows_map(&tk, no_keys ? q : k, d, no_keys ? H_q : H_kv, no_keys ? s.q_rows : s.k_rows,
+                      s.q_batch) != ATTN_OK ||
+      encode_rows_map(&tv, no_keys ? q : v, d, no_keys ? H_q : H_kv, no_keys ? s.q_rows : s.k_rows,
+                      s.q_batch) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+
+  FwdParams p;
+  p.o = o;
+  p.lse = lse;
+  p.cu_seqlens = seqlens;
+  p.B = B; p.H_q = H_q; p.H_kv = H_kv; p.N_q = N_q; p.N_k = N_k;
+  p.group = H_q / H_kv;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * kLog2e;
+  p.err = err;
+  p.wait_limit = g_wait_limit;
+  dim3 grid;
+  if (seqlens) {
+    // upper bound on sum over sequences of ceil(L / 256)
+    const long long ub = (static_cast<long long>(N_q) + 255ll * B) / 256;
+    if (ub > 0x7fffffffll) return ATTN_ERR_BAD_SHAPE;
+    p.n_mblocks = static_cast<int>(ub);
+    grid = dim3(static_cast<unsigned>(ub), H_q, 1);
+  } else {
+    p.n_mblocks = (N_q + 255) / 256;
+    grid = dim3(p.n_mblocks, H_q, B);
+  }
+  if (launch_attn_fwd(d, tq, tk, tv, p, grid, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int N_q, int N_k, int d, int varlen,
+                                int deterministic) {
+  Shape s;
+  if (check_shape(B, H_q, H_kv, N_q, N_k, d, 0, varlen ? reinterpret_cast<const int*>(16) : nullptr,
+                  &s) != ATTN_OK)
+    return 0;
+  BwdPlan pl;
+  if (!bwd_plan(B, H_q, H_kv, N_q, N_k, d, varlen != 0, deterministic != 0, &pl)) return 0;
+  return pl.total;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int N_q,
+             int N_k, int d, int causal, const int* seqlens, float scale, int deterministic,
+             void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  Shape s;
+  int st = check_shape(B, H_q, H_kv, N_q, N_k, d, causal, seqlens, &s);
+  if (st != ATTN_OK) return st;
+  const bool has_q = B > 0 && N_q > 0, has_k = B > 0 && N_k > 0;
+  if ((has_q && (!q || !o || !lse || !dout || !dq)) || (has_k && (!k || !v || !dk || !dv)))
+    return ATTN_ERR_NULL_PTR;
+  if (!std::isfinite(scale)) return ATTN_ERR_BAD_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (seqlens && (reinterpret_cast<uintptr_t>(seqlens) & 3u)))
+    return ATTN_ERR_ALIGNMENT;
+  BwdPlan pl;
+  if (!bwd_plan(B, H_q, H_kv, N_q, N_k, d, seqlens != nullptr, deterministic != 0, &pl))
+    return ATTN_ERR_BAD_SHAPE;
+  if (B == 0) return ATTN_OK;
+  int dev;
+  if ((st = current_device(&dev)) != ATTN_OK) return st;
+  int* err = nullptr;
+  if ((st = device_setup(dev, &err)) != ATTN_OK) return st;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const size_t q_bytes = static_cast<size_t>(pl.rows_q) * H_q * d * 2;
+  const size_t k_bytes = static_cast<size_t>(s.varlen ? N_k : static_cast<long long>(B) * N_k) * H_kv * d * 2;
+  if (N_q == 0 || N_k == 0) {
+    // no query rows: no key gradient; no keys: every row sees nothing
+    if ((q_bytes && cudaMemsetAsync(dq, 0, q_bytes, cs) != cudaSuccess) ||
+        (k_bytes && cudaMemsetAsync(dk, 0, k_bytes, cs) != cudaSuccess) ||
+        (k_bytes && cudaMemsetAsync(dv, 0, k_bytes, cs) != cudaSuccess))
+      return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  if (workspace == nullptr || workspace_bytes < pl.total) return ATTN_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGNMENT;
+
+  CUtensorMap maps[4];
+  if (encode_rows_map(&maps[0], q, d, H_q, s.q_rows, s.q_batch) != ATTN_OK ||
+      encode_rows_map(&maps[1], k, d, H_kv, s.k_rows, s.q_batch) != ATTN_OK ||
+      encode_rows_map(&maps[2], v, d, H_kv, s.k_rows, s.q_batch) != ATTN_OK ||
+      encode_rows_map(&maps[3], dout, d, H_q, s.q_rows, s.q_batch) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  BwdParams p;
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.dout = dout;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  p.dq_acc = reinterpret_cast<float*>(ws + pl.acc_off);
+  p.dvec = reinterpret_cast<float*>(ws + pl.dvec_off);
+  p.sem = deterministic ? reinterpret_cast<int*>(ws + pl.sem_off) : nullptr;
+  p.cu_seqlens = seqlens;
+  p.B = B; p.H_q = H_q; p.H_kv = H_kv; p.N_q = N_q; p.N_k = N_k; p.group = H_q / H_kv; p.d = d;
+  p.causal = causal ? 1 : 0;
+  p.deterministic = deterministic ? 1 : 0;
+  p.n_nblocks = 0;
+  p.n_mtiles = 0;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.err = err;
+  p.wait_limit = g_wait_limit;
+  const int n_sem = static_cast<int>(pl.slots * H_q);
+  if (launch_attn_bwd(p, maps, cs, pl.rows_q, n_sem, static_cast<int>(pl.n_work)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+int attn_check(attn_stream_t stream) {
+  int dev;
+  int st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  int* err = nullptr;
+  if ((st = device_setup(dev, &err)) != ATTN_OK) return st;
+  int h = 0;
+  if (cudaMemcpy(&h, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (h != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    return ATTN_ERR_TIMEOUT;
+  }
+  return ATTN_OK;
+}
+
+int attn_debug_exp2(const float* x, float* y, int n, int mode, attn_stream_t stream) {
+  if (n < 0) return ATTN_ERR_BAD_SHAPE;
+  if (n > 0 && (!x || !y)) return ATTN_ERR_NULL_PTR;
+  int dev;
+  int st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  int* err;
+  if ((st = device_setup(dev, &err)) != ATTN_OK) return st;
+  return launch_exp2_probe(x, y, n, mode ? 1 : 0, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_CUDA;
+}
+
+}  // extern "C"

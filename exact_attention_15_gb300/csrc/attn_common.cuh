@@ -1,0 +1,86 @@
+// Shared definitions of the attention kernels: launch parameters, tile sizes,
+// the FMA-pipe exp2 and the device error word.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr int kTileM = 128;   // query rows per tile (tcgen05 M)
+constexpr int kTileN = 128;   // keys per tile
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// Conditional rescaling threshold, in powers of two: the running max used for
+// the exponentials is only moved when the true max has grown by more than
+// 2^8 = 256 (FlashAttention-4 summary, section 3.1.4).
+constexpr float kTau = 8.0f;
+
+enum DevErr : int { kErrNone = 0, kErrTimeout = 1 };
+
+struct FwdParams {
+  void* o;              // bf16
+  float* lse;
+  const int* cu_seqlens;  // nullptr for fixed length
+  int B, H_q, H_kv, N_q, N_k, group;
+  int causal;
+  int n_mblocks;        // CTA tiles (2 x 128 query rows) per (batch, head) or upper bound (packed)
+  float scale_log2;     // scale * log2(e)
+  int* err;             // device error word
+  long long wait_limit; // cycles
+};
+
+struct BwdParams {
+  const void* q; const void* k; const void* v; const void* o; const float* lse;
+  const void* dout;
+  void* dq; void* dk; void* dv;
+  float* dq_acc;        // fp32 [rows, H_q, d]
+  float* dvec;          // fp32 D, laid out like lse
+  int* sem;             // deterministic mode: one counter per (b, h_q, query tile)
+  const int* cu_seqlens;
+  int B, H_q, H_kv, N_q, N_k, group, d;
+  int causal, deterministic;
+  int n_nblocks;        // key tiles per (batch, kv head) or upper bound (packed)
+  int n_mtiles;         // query tiles per (batch, head) (fixed length) or upper bound
+  float scale, scale_log2;
+  int* err;
+  long long wait_limit;
+};
+
+// Kernel tracing (host side, implemented next to the C ABI). prof_begin
+// returns a slot (or -1 when tracing is off); prof_end closes it.
+enum KernelId : int { kKFwd = 1, kKBwdPre = 2, kKBwdMain = 3, kKBwdPost = 4, kKExp2 = 5 };
+int prof_begin(int kernel, cudaStream_t stream);
+void prof_end(int slot, cudaStream_t stream);
+
+// Records the first device-side failure; never traps.
+__device__ __forceinline__ void record_error(int* err, int code) {
+  if (err != nullptr) atomicCAS(err, 0, code);
+}
+
+// 2^x on the FMA pipe: Cody-Waite split x = floor(x) + f, f in [0, 1), a
+// degree-3 minimax polynomial for 2^f (coefficients fitted by
+// fit_exp2_poly.py, max relative error 8.6e-5 on [0, 1)), and the integer part
+// added straight into the exponent field (FlashAttention-4 summary, 3.1.3).
+// x is clamped at -127 so the exponent arithmetic cannot underflow; callers
+// must not pass -inf for an element that has to come out as exactly 0.
+__device__ __forceinline__ float exp2_poly3(float x) {
+  constexpr float kC1 = 0.6951167583465576f;
+  constexpr float kC2 = 0.22764499485492706f;
+  constexpr float kC3 = 0.07706703990697861f;
+  constexpr float kShift = 12582912.0f;  // 2^23 + 2^22
+  x = fmaxf(x, -127.0f);
+  const float t = __fadd_rd(x, kShift);          // kShift + floor(x), exactly
+  const float f = x - (t - kShift);              // fraction in [0, 1)
+  const int e = __float_as_int(t) - __float_as_int(kShift);  // floor(x)
+  float p = fmaf(kC3, f, kC2);
+  p = fmaf(p, f, kC1);
+  p = fmaf(p, f, 1.0f);
+  return __int_as_float(__float_as_int(p) + (e << 23));
+}
+
+}  // namespace attn

@@ -1,0 +1,467 @@
+// Forward pass of exact softmax attention for sm_103a.
+//
+// One CTA owns two 128-row query tiles of one (batch, query head) and streams
+// every key/value tile they see through shared memory
+// (FlashAttention-4 summary, section 3.1.2: two output tiles per CTA, one
+// softmax warpgroup per tile, one thread per row; the FlashAttention-2 loop order
+// with the query tile outside and keys/values inside).
+//
+// Warp roles (384 threads):
+//   warp 0      TMA producer: both Q tiles once, then K_j / V_j into a ring of
+//               single-tile stages (order K0 V0 K1 V1 ...).
+//   warp 1      TMEM owner and MMA issuer (one thread): S_t = Q_t K_j^T (SS) and
+//               O_t += P_t V_j (TS, P read from TMEM), ping-ponging the tiles so
+//               the tensor core works on one tile while the other is in softmax.
+//   warps 4-7   softmax for tile 0, warps 8-11 softmax for tile 1: load the S row
+//               from TMEM, mask, row max, conditional rescale (tau = 8 in powers
+//               of two, decided per warp), exp2, row sum, P (bf16) back into the S
+//               columns of TMEM, and finally the epilogue O / l and LSE.
+//
+// TMEM (512 columns): O_0 [0, d), O_1 [d, 2d), S_0/P_0 [2d, 2d+128),
+// S_1/P_1 [2d+128, 2d+256).
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "attn_common.cuh"
+
+namespace attn {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kHalves = D / 64;                 // 128-byte column blocks per row
+  static constexpr int kTileBytes = kTileM * D * 2;      // one 128-row bf16 tile
+  static constexpr int kStages = (D == 128) ? 4 : 8;     // K/V ring, one tile per stage
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+  static constexpr uint32_t kColO0 = 0, kColO1 = D;
+  static constexpr uint32_t kColS0 = 2 * D, kColS1 = 2 * D + 128;
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+struct FwdBars {
+  uint64_t q_full;
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  uint32_t tmem_base;
+};
+
+// Work decode shared by every role of the CTA.
+struct FwdTile {
+  int b, h, h_kv;
+  int q0;          // first query row of tile 0, relative to the sequence
+  int row_base;    // global packed-row offset of the sequence (0 for fixed length)
+  int batch_coord; // TMA batch coordinate (b for fixed length, 0 for packed)
+  int Lq, Lk;
+  int n[2];        // key tiles each query tile visits
+  int valid[2];
+};
+
+__device__ __forceinline__ bool decode_fwd_tile(const FwdParams& p, FwdTile& t) {
+  t.h = blockIdx.y;
+  t.h_kv = t.h / p.group;
+  int m;
+  if (p.cu_seqlens == nullptr) {
+    t.b = blockIdx.z;
+    m = p.causal ? (p.n_mblocks - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+    t.row_base = 0;
+    t.batch_coord = t.b;
+    t.Lq = p.N_q;
+    t.Lk = p.N_k;
+  } else {
+    int idx = blockIdx.x;
+    int s = 0;
+    int L = 0;
+    for (; s < p.B; ++s) {
+      L = p.cu_seqlens[s + 1] - p.cu_seqlens[s];
+      const int nt = (L + 2 * kTileM - 1) / (2 * kTileM);
+      if (idx < nt) break;
+      idx -= nt;
+    }
+    if (s >= p.B) return false;
+    const int nt = (L + 2 * kTileM - 1) / (2 * kTileM);
+    m = p.causal ? (nt - 1 - idx) : idx;
+    t.b = s;
+    t.row_base = p.cu_seqlens[s];
+    t.batch_coord = 0;
+    t.Lq = L;
+    t.Lk = L;
+  }
+  t.q0 = m * 2 * kTileM;
+  for (int i = 0; i < 2; ++i) {
+    const int r0 = t.q0 + i * kTileM;
+    t.valid[i] = r0 < t.Lq;
+    int kv_end = t.Lk;
+    if (p.causal) kv_end = min(kv_end, r0 + kTileM);
+    t.n[i] = t.valid[i] ? (kv_end + kTileN - 1) / kTileN : 0;
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------ softmax
+template <int D, int EMU, bool POS_SCALE>
+__device__ __forceinline__ void softmax_row_tile(float (&s)[128], float c, float& m_used,
+                                                 float& l, int kv0, int qrow, const FwdTile& t,
+                                                 bool need_mask, int causal,
+                                                 uint32_t (&pk)[64], bool& rescale_warp,
+                                                 float& factor) {
+  if (!POS_SCALE) {
+#pragma unroll
+    for (int i = 0; i < 128; ++i) s[i] *= c;
+  }
+  if (need_mask) {
+#pragma unroll
+    for (int i = 0; i < 128; ++i) {
+      const int key = kv0 + i;
+      const bool vis = key < t.Lk && (!causal || key <= qrow);
+      s[i] = vis ? s[i] : -INFINITY;
+    }
+  }
+  float mx[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+  for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+  float m = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+  if (POS_SCALE) m *= c;  // max of the scaled scores (c > 0)
+  const float m_new = fmaxf(m_used, m);
+  const bool need = (m_new - m_used) > kTau;  // false when both are -inf (NaN compare)
+  rescale_warp = __any_sync(0xffffffffu, need);
+  factor = 1.0f;
+  if (rescale_warp) {
+    if (m_new > m_used) {
+      factor = ex2_approx(m_used - m_new);  // 0 when m_used = -inf
+      m_used = m_new;
+      l *= factor;
+    }
+  }
+  const float mb = (m_used == -INFINITY) ? 0.0f : m_used;
+  float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    float x0, x1;
+    if (POS_SCALE) {
+      x0 = fmaf(s[2 * i], c, -mb);
+      x1 = fmaf(s[2 * i + 1], c, -mb);
+    } else {
+      x0 = s[2 * i] - mb;
+      x1 = s[2 * i + 1] - mb;
+    }
+    float p0, p1;
+    if (EMU > 0 && !need_mask && (i & 7) >= 8 - EMU) {
+      p0 = exp2_poly3(x0);
+      p1 = exp2_poly3(x1);
+    } else {
+      p0 = ex2_approx(x0);
+      p1 = ex2_approx(x1);
+    }
+    sum[i & 3] += p0 + p1;
+    pk[i] = pack_bf16x2(p0, p1);
+  }
+  l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+}
+
+template <int D, int EMU>
+__global__ void __launch_bounds__(384, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using Cfg = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  FwdBars* bars = reinterpret_cast<FwdBars*>(smem + Cfg::kBarOff);
+
+  FwdTile t;
+  if (!decode_fwd_tile(p, t)) return;  // packed inputs: grid is an upper bound
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  if (tid == 0) {
+    mbar_init(smem_addr(&bars->q_full), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(&bars->s_full[i]), 1);
+      mbar_init(smem_addr(&bars->p_full[i]), 128);
+      mbar_init(smem_addr(&bars->pv_done[i]), 1);
+    }
+    for (int i = 0; i < Cfg::kStages; ++i) {
+      mbar_init(smem_addr(&bars->kv_full[i]), 1);
+      mbar_init(smem_addr(&bars->kv_empty[i]), 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&bars->tmem_base), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const int n_kv = max(t.n[0], t.n[1]);
+  const long long lim = p.wait_limit;
+
+  // Register split: 128 x 56 (warps 0-3) + 256 x 224 (softmax) = 384 x 168.
+  // Each budget change sits inside the branch of the warps it applies to, so the
+  // compiler sees which code runs under which budget.
+  if (warp < 4) {
+    regs_dec<56>();
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0 && n_kv > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const uint32_t qbar = smem_addr(&bars->q_full);
+      const int nq = (t.n[0] > 0) + (t.n[1] > 0);
+      mbar_arrive_expect_tx(qbar, nq * Cfg::kTileBytes);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (t.n[i] == 0) continue;
+        const uint32_t dst = smem_addr(smem + Cfg::kQOff + i * Cfg::kTileBytes);
+        for (int hf = 0; hf < Cfg::kHalves; ++hf)
+          tma_load_4d(dst + hf * 16384, &tm_q, qbar, hf * 64, t.h, t.row_base + t.q0 + i * kTileM,
+                      t.batch_coord);
+      }
+      for (int it = 0; it < 2 * n_kv; ++it) {
+        const int j = it >> 1;
+        const int stage = it % Cfg::kStages;
+        const int round = it / Cfg::kStages;
+        if (!mbar_wait(smem_addr(&bars->kv_empty[stage]), (round & 1) ^ 1, lim)) {
+          record_error(p.err, kErrTimeout);
+          break;
+        }
+        const uint32_t fbar = smem_addr(&bars->kv_full[stage]);
+        mbar_arrive_expect_tx(fbar, Cfg::kTileBytes);
+        const uint32_t dst = smem_addr(smem + Cfg::kKVOff + stage * Cfg::kTileBytes);
+        const CUtensorMap* map = (it & 1) ? &tm_v : &tm_k;
+        for (int hf = 0; hf < Cfg::kHalves; ++hf)
+          tma_load_4d(dst + hf * 16384, map, fbar, hf * 64, t.h_kv, t.row_base + j * kTileN,
+                      t.batch_coord);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_kv > 0) {
+      constexpr uint32_t kIdS = make_idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t kIdPV = make_idesc_bf16(128, D, 0, 1);
+      const uint32_t q_base = smem_addr(smem + Cfg::kQOff);
+      const uint32_t kv_base = smem_addr(smem + Cfg::kKVOff);
+      bool ok = mbar_wait(smem_addr(&bars->q_full), 0, lim);
+      auto issue_s = [&](int i, int stage) {
+        const uint32_t qa = q_base + i * Cfg::kTileBytes;
+        const uint32_t kb = kv_base + stage * Cfg::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + Cfg::kColS0 + i * 128, make_sdesc_sw128(qa + off, 16, 1024),
+                 make_sdesc_sw128(kb + off, 16, 1024), kIdS, kk > 0);
+        }
+        mma_commit(smem_addr(&bars->s_full[i]));
+      };
+      auto issue_pv = [&](int i, int stage, int j) {
+        const uint32_t vb = kv_base + stage * Cfg::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          mma_ts(tmem + Cfg::kColO0 + i * D, tmem + Cfg::kColS0 + i * 128 + kk * 8,
+                 make_sdesc_sw128(vb + kk * 2048, 16384, 1024), kIdPV, (j > 0 || kk > 0));
+        }
+        mma_commit(smem_addr(&bars->pv_done[i]));
+      };
+      // K_j is load number 2j, V_j load number 2j+1.
+      auto stage_of = [&](int it) { return it % Cfg::kStages; };
+      auto phase_of = [&](int it) { return (it / Cfg::kStages) & 1; };
+      if (ok) ok = mbar_wait(smem_addr(&bars->kv_full[stage_of(0)]), phase_of(0), lim);
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          if (t.n[i] > 0) issue_s(i, stage_of(0));
+        mma_commit(smem_addr(&bars->kv_empty[stage_of(0)]));
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int itv = 2 * j + 1, itk = 2 * j + 2;
+        const bool next_k = (j + 1) < n_kv;
+        ok = mbar_wait(smem_addr(&bars->kv_full[stage_of(itv)]), phase_of(itv), lim);
+        if (ok && next_k) ok = mbar_wait(smem_addr(&bars->kv_full[stage_of(itk)]), phase_of(itk), lim);
+        if (!ok) break;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if (j >= t.n[i]) continue;
+          if (!mbar_wait(smem_addr(&bars->p_full[i]), j & 1, lim)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(i, stage_of(itv), j);
+          if (j + 1 < t.n[i]) issue_s(i, stage_of(itk));
+        }
+        if (!ok) break;
+        mma_commit(smem_addr(&bars->kv_empty[stage_of(itv)]));
+        if (next_k) mma_commit(smem_addr(&bars->kv_empty[stage_of(itk)]));
+      }
+      if (!ok) record_error(p.err, kErrTimeout);
+    }
+  }
+    __syncwarp();
+  } else {
+    regs_inc<224>();
+    // ---------------------------------------------------------- softmax + epilogue
+    const int i = (warp - 4) >> 2;          // query tile of this warpgroup
+    const int r = tid - 128 * (1 + i);      // row within the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((r & ~31)) << 16;
+    const uint32_t col_s = i ? Cfg::kColS1 : Cfg::kColS0;
+    const uint32_t col_o = i ? Cfg::kColO1 : Cfg::kColO0;
+    const int qrow = t.q0 + i * kTileM + r;  // sequence-relative query row
+    const int my_n = i ? t.n[1] : t.n[0];
+    const int my_valid = i ? t.valid[1] : t.valid[0];
+    const float c = p.scale_log2;
+    float m_used = -INFINITY;
+    float l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < my_n; ++j) {
+      if (!mbar_wait(smem_addr(&bars->s_full[i]), j & 1, lim)) { ok = false; break; }
+      tc_fence_after();
+      float s[128];
+      {
+        uint32_t* sr = reinterpret_cast<uint32_t*>(s);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          tmem_ld32(tmem + lane_base + col_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + cc * 32));
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + cc * 32));
+      }
+      const int kv0 = j * kTileN;
+      const bool need_mask = (kv0 + kTileN > t.Lk) || (p.causal && kv0 + kTileN - 1 > t.q0 + i * kTileM);
+      uint32_t pk[64];
+      bool rescale_warp;
+      float factor;
+      if (c > 0.0f)
+        softmax_row_tile<D, EMU, true>(s, c, m_used, l, kv0, qrow, t, need_mask, p.causal, pk,
+                                       rescale_warp, factor);
+      else
+        softmax_row_tile<D, 0, false>(s, c, m_used, l, kv0, qrow, t, need_mask, p.causal, pk,
+                                      rescale_warp, factor);
+      if (rescale_warp && j > 0 && __any_sync(0xffffffffu, factor != 1.0f)) {
+        // correction: O_{j-1} must be complete before it is scaled
+        if (!mbar_wait(smem_addr(&bars->pv_done[i]), (j - 1) & 1, lim)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + col_o + cc * 32, ov);
+          tmem_ld_wait(ov);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
+          tmem_st32(tmem + lane_base + col_o + cc * 32, ov);
+        }
+      }
+      tmem_st32(tmem + lane_base + col_s, *reinterpret_cast<uint32_t(*)[32]>(pk));
+      tmem_st32(tmem + lane_base + col_s + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_addr(&bars->p_full[i]));
+    }
+    if (!ok) record_error(p.err, kErrTimeout);
+    // ---------------------------------------------------------- epilogue
+    if (my_valid) {
+      bool have_o = ok && my_n > 0;
+      if (have_o) {
+        have_o = mbar_wait(smem_addr(&bars->pv_done[i]), (my_n - 1) & 1, lim);
+        if (!have_o) record_error(p.err, kErrTimeout);
+        tc_fence_after();
+      }
+      const bool row_ok = qrow < t.Lq;
+      const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
+      const size_t grow = static_cast<size_t>(t.row_base) + qrow;  // packed row
+      const size_t o_off =
+          p.cu_seqlens ? (grow * p.H_q + t.h) * D
+                       : ((static_cast<size_t>(t.b) * p.N_q + qrow) * p.H_q + t.h) * D;
+      uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + o_off);
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t ov[32];
+        if (have_o) {
+          tmem_ld32(tmem + lane_base + col_o + cc * 32, ov);
+          tmem_ld_wait(ov);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = 0u;
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            orow[cc * 4 + e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        }
+      }
+      if (row_ok) {
+        const float lse = (l > 0.0f) ? (m_used * kLn2 + __logf(l)) : -INFINITY;
+        const size_t l_off = p.cu_seqlens
+                                 ? static_cast<size_t>(t.h) * p.N_q + grow
+                                 : (static_cast<size_t>(t.b) * p.H_q + t.h) * p.N_q + qrow;
+        p.lse[l_off] = lse;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+template <int D, int EMU>
+static cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, const FwdParams& p, dim3 grid,
+                                   cudaStream_t stream) {
+  using Cfg = FwdCfg<D>;
+  auto kern = attn_fwd_kernel<D, EMU>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int slot = prof_begin(kKFwd, stream);
+  kern<<<grid, 384, Cfg::kSmemBytes, stream>>>(tq, tk, tv, p);
+  e = cudaGetLastError();
+  prof_end(slot, stream);
+  return e;
+}
+
+// Number of exponentials per 8 pairs routed to the FMA polynomial.
+#ifndef ATTN_FWD_EMU
+#define ATTN_FWD_EMU 0
+#endif
+
+cudaError_t launch_attn_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const FwdParams& p, dim3 grid,
+                            cudaStream_t stream) {
+  if (d == 64) return launch_fwd_impl<64, ATTN_FWD_EMU>(tq, tk, tv, p, grid, stream);
+  return launch_fwd_impl<128, ATTN_FWD_EMU>(tq, tk, tv, p, grid, stream);
+}
+
+// ------------------------------------------------------------------ exp2 test hook
+__global__ void exp2_probe_kernel(const float* __restrict__ x, float* __restrict__ y, int n,
+                                  int mode) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) y[i] = mode ? exp2_poly3(x[i]) : ex2_approx(x[i]);
+}
+
+cudaError_t launch_exp2_probe(const float* x, float* y, int n, int mode, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  const int slot = prof_begin(kKExp2, stream);
+  exp2_probe_kernel<<<(n + 255) / 256, 256, 0, stream>>>(x, y, n, mode);
+  const cudaError_t e = cudaGetLastError();
+  prof_end(slot, stream);
+  return e;
+}
+
+}  // namespace attn

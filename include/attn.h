@@ -1,0 +1,165 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact softmax attention library.
+ *
+ * The operation (FlashAttention-4 summary, papercache.org, section 2.1; the
+ * FlashAttention explainer, wq-win.github.io, section 2): for every batch entry b
+ * and query head h,
+ *
+ *     S = scale * Q K^T + mask,   P = softmax(S) row by row,   O = P V,
+ *     LSE_i = ln sum_j exp(S_ij)            (natural log, of the scaled scores)
+ *
+ * computed tile by tile with the online-softmax (m, l, u) merge so that S and P
+ * never reach device memory; and its gradient (same section 2.1):
+ *
+ *     D = rowsum(dO o O),  dP = dO V^T,  dS = P o (dP - D),
+ *     dV = P^T dO,  dQ = scale * dS K,  dK = scale * dS^T Q,
+ *
+ * with P rebuilt from the saved LSE (recomputation: FlashAttention notes,
+ * xwysyy.cn, "Recomputation").
+ *
+ * Masks: causal means query i sees key j only when j <= i. Grouped-query
+ * attention: query head h reads KV head h / (H_q / H_kv); dK and dV of a KV head
+ * are summed over the query heads that read it.
+ *
+ * Data types and layouts. q, k, v, o, dout, dq, dk, dv are bf16 (raw 16-bit
+ * storage, passed as void*), row-major and contiguous, head dimension innermost:
+ *   fixed length (seqlens == NULL):
+ *       q, o, dout, dq : [B, N_q, H_q, d]     k, v, dk, dv : [B, N_k, H_kv, d]
+ *       lse            : float [B, H_q, N_q]
+ *   packed variable length (seqlens != NULL):
+ *       seqlens        : device int32 cu_seqlens[B + 1], cu_seqlens[0] = 0,
+ *                        non-decreasing; sequence s owns rows
+ *                        cu_seqlens[s] .. cu_seqlens[s+1]-1 of q AND of k/v
+ *                        (self-attention: one offset array for both)
+ *       B              : number of sequences
+ *       N_q = N_k      : total packed rows T = cu_seqlens[B]
+ *       q, o, dout, dq : [T, H_q, d]          k, v, dk, dv : [T, H_kv, d]
+ *       lse            : float [H_q, T]
+ *   Supported head dimensions: d = 64 and d = 128. Every pointer must be 16-byte
+ *   aligned (tensor-memory-accelerator copies need it).
+ *
+ * Ownership and execution. The caller allocates and owns every buffer; the
+ * library never frees caller memory and, apart from attn_bwd's caller-provided
+ * workspace, uses no device memory of its own except one error word per
+ * device. Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t;
+ * NULL is the legacy default stream); none synchronises the host.
+ *
+ * Errors. Argument errors are detected on the host before anything is launched
+ * and return a non-zero attn_status; no exception crosses the ABI. A launch
+ * failure returns ATTN_ERR_CUDA. Device-side pipeline waits are bounded: if one
+ * ever runs out of time the kernel records ATTN_ERR_TIMEOUT in the device error
+ * word and returns; attn_check() reports (and clears) it.
+ */
+#ifndef ATTN_H_
+#define ATTN_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* attn_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_NULL_PTR = 1,             /* a required pointer is NULL */
+  ATTN_ERR_ALIGNMENT = 2,            /* a tensor pointer is not 16-byte aligned */
+  ATTN_ERR_UNSUPPORTED_HEADDIM = 3,  /* d not in {64, 128} */
+  ATTN_ERR_BAD_SHAPE = 4,            /* a size is negative, too large, or inconsistent */
+  ATTN_ERR_GQA_RATIO = 5,            /* H_q not a positive multiple of H_kv */
+  ATTN_ERR_CAUSAL_SHAPE = 6,         /* causal with N_q != N_k (alignment undefined) */
+  ATTN_ERR_WORKSPACE = 7,            /* workspace NULL or smaller than required */
+  ATTN_ERR_CUDA = 8,                 /* a CUDA runtime call or launch failed */
+  ATTN_ERR_TIMEOUT = 9,              /* a device-side bounded wait ran out */
+  ATTN_ERR_NO_DEVICE = 10,           /* no usable CUDA device */
+  ATTN_ERR_UNSUPPORTED_DEVICE = 11   /* device is not sm_103 (GB300-class) */
+} attn_status;
+
+/*
+ * Forward pass: writes O (bf16) and LSE (fp32, natural log) for every query row.
+ * scale is the score multiplier alpha (1/sqrt(d) in the usual definition; any
+ * finite value is accepted). A query row that sees no key (only possible with
+ * empty sequences) gets O = 0 and LSE = -inf.
+ * FlashAttention-4 summary, sections 2.1 (definition), 3.1.2 (pipeline),
+ * 3.1.4 (online softmax with conditional rescaling).
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int H_q, int H_kv, int N_q, int N_k, int d, int causal,
+             const int* seqlens, float scale, attn_stream_t stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs for these sizes (0 on invalid
+ * sizes). Arguments mean what they mean for attn_bwd; `varlen` is non-zero when
+ * attn_bwd will be given a cu_seqlens array (then N_q is the packed row count).
+ * The workspace holds the fp32 dQ accumulator [rows, H_q, d], D = rowsum(dO o O)
+ * (laid out like lse) and, in deterministic mode, one ordering semaphore per
+ * (query tile, query head) plus a work counter.
+ */
+size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int N_q, int N_k, int d, int varlen,
+                                int deterministic);
+
+/*
+ * Backward pass: given q, k, v, the forward outputs o and lse, and the output
+ * gradient dout, writes dq [like q], dk and dv [like k] (bf16, overwritten, not
+ * accumulated into). `workspace` is caller-owned device memory of at least
+ * attn_bwd_workspace_bytes(...) bytes, 256-byte aligned; its contents on entry
+ * do not matter and are undefined on return. With deterministic != 0 the dQ
+ * reduction across key tiles runs in a fixed order, so dq, dk and dv are
+ * bit-identical across runs with the same inputs on the same device.
+ * FlashAttention-4 summary, sections 2.1 (gradients), 3.2.2 (pipeline),
+ * 3.2.4 (deterministic mode).
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv,
+             int B, int H_q, int H_kv, int N_q, int N_k, int d, int causal,
+             const int* seqlens, float scale, int deterministic,
+             void* workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns ATTN_ERR_TIMEOUT if a kernel of this
+ * library on the current device recorded a timed-out wait since the last check
+ * (and clears the record), ATTN_ERR_CUDA if the stream reports an error, else
+ * ATTN_OK.
+ */
+int attn_check(attn_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* attn_status_string(int status);
+
+/*
+ * Test hook for the FMA-pipe exp2 used inside the forward kernel: y[i] =
+ * 2^x[i] computed with mode 0 = the hardware ex2.approx instruction, mode 1 =
+ * the degree-3 polynomial emulation (FlashAttention-4 summary, section 3.1.3).
+ * x and y are device float arrays of n elements.
+ */
+int attn_debug_exp2(const float* x, float* y, int n, int mode, attn_stream_t stream);
+
+/*
+ * Sets the cycle budget of every bounded device-side wait for later launches
+ * on this process (default about one second of SM clock). Returns the old value.
+ */
+long long attn_set_wait_limit(long long cycles);
+
+/*
+ * Kernel tracing. While enabled (process-wide), every kernel this library
+ * launches is bracketed by two CUDA events recorded on the launching stream.
+ * attn_profile_read() waits for the recorded events, copies up to
+ * `max_records` records (oldest first) and discards everything it has read;
+ * it returns the number of records written, or a negative attn_status.
+ * Kernel ids: 1 forward, 2 backward pre (D, zeroing), 3 backward main,
+ * 4 backward post (dQ conversion), 5 exp2 test hook.
+ */
+typedef struct {
+  int kernel;  /* kernel id, see above */
+  float ms;    /* elapsed time between the two events */
+} attn_profile_record;
+
+int attn_profile_enable(int enable);
+int attn_profile_read(attn_profile_record* out, int max_records);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H_ */

@@ -1,0 +1,205 @@
+"""GPU parity: the CUDA forward and backward passes against the fp64 oracle on
+the same seeded bf16 inputs, through the C ABI (ctypes binding).
+
+Small cases are compared element by element in full; they span several tiles
+and a ragged tail. The five named workloads run at full size on the GPU and are
+compared on seeded (batch, head) samples (every row of a sampled head, or a
+seeded subset of rows for the longest sequences).
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from exact_attention_15_gb300 import workloads as W
+from gpu_common import (GRAD_TOL, LSE_TOL, O_TOL, as_f64, gpu_head, gpu_lse, head_slices,
+                        rel_fro, run_backward, run_forward, to_host_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_fwd_check(inp, o, lse, pairs, rows=None):
+    worst_o = worst_l = 0.0
+    for b, h in pairs:
+        q, k, v, _ = head_slices(inp, b, h)
+        if q.shape[0] == 0:
+            continue
+        r = None
+        if rows is not None:
+            r = np.unique(np.concatenate([rows[rows < q.shape[0]], [q.shape[0] - 1]]))
+        o_ref, lse_ref = oracle.head_forward(q, k, v, inp.scale, inp.causal, rows=r)
+        o_gpu = gpu_head(o, inp, b, h)
+        l_gpu = gpu_lse(lse, inp, b, h)
+        if r is not None:
+            o_gpu, l_gpu = o_gpu[r], l_gpu[r]
+        fin = np.isfinite(lse_ref)
+        assert np.array_equal(fin, np.isfinite(l_gpu)), "masked-row pattern differs"
+        worst_o = max(worst_o, float(np.max(np.abs(o_gpu - o_ref))) if o_ref.size else 0.0)
+        if fin.any():
+            worst_l = max(worst_l, float(np.max(np.abs(l_gpu[fin] - lse_ref[fin]))))
+    assert worst_o <= O_TOL, f"O max-abs error {worst_o}"
+    assert worst_l <= LSE_TOL, f"LSE abs error {worst_l}"
+    return worst_o, worst_l
+
+
+def _oracle_bwd_check(inp, dq, dk, dv, groups):
+    g = inp.H_q // inp.H_kv
+    worst = 0.0
+    for b, hk in groups:
+        dk_ref = dv_ref = None
+        for h in range(hk * g, (hk + 1) * g):
+            q, k, v, do = head_slices(inp, b, h)
+            if q.shape[0] == 0:
+                continue
+            r = oracle.head_backward(q, k, v, do, inp.scale, inp.causal)
+            e = rel_fro(gpu_head(dq, inp, b, h), r["dq"])
+            assert e <= GRAD_TOL, f"dQ rel err {e} (b={b}, h={h})"
+            worst = max(worst, e)
+            dk_ref = r["dk"] if dk_ref is None else dk_ref + r["dk"]
+            dv_ref = r["dv"] if dv_ref is None else dv_ref + r["dv"]
+        if dk_ref is None:
+            continue
+        ek = rel_fro(gpu_head(dk, inp, b, hk), dk_ref)
+        ev = rel_fro(gpu_head(dv, inp, b, hk), dv_ref)
+        assert ek <= GRAD_TOL, f"dK rel err {ek} (b={b}, kv head={hk})"
+        assert ev <= GRAD_TOL, f"dV rel err {ev} (b={b}, kv head={hk})"
+        worst = max(worst, ek, ev)
+    return worst
+
+
+def _all_pairs(inp):
+    return [(b, h) for b in range(inp.B) for h in range(inp.H_q)]
+
+
+def _all_groups(inp):
+    return [(b, g) for b in range(inp.B) for g in range(inp.H_kv)]
+
+
+SMALL = {
+    "tiny_cfg": dict(B=1, H_q=1, H_kv=1, N_q=128, N_k=128, d=64, scale=1 / math.sqrt(8), causal=False),
+    "ragged_d64": dict(B=2, H_q=2, H_kv=2, N_q=300, N_k=300, d=64, causal=False),
+    "ragged_d128_causal": dict(B=2, H_q=2, H_kv=2, N_q=300, N_k=300, d=128, causal=True),
+    "gqa_causal": dict(B=1, H_q=4, H_kv=2, N_q=257, N_k=257, d=128, causal=True),
+    "cross_lengths": dict(B=2, H_q=1, H_kv=1, N_q=200, N_k=333, d=64, causal=False),
+    "one_query_row": dict(B=1, H_q=2, H_kv=1, N_q=1, N_k=700, d=128, causal=False),
+    "varlen_causal": dict(B=0, H_q=4, H_kv=1, N_q=0, N_k=0, d=128, causal=True,
+                          seqlens=[1, 127, 129, 300, 513, 64]),
+    "varlen_d64": dict(B=0, H_q=2, H_kv=2, N_q=0, N_k=0, d=64, causal=False, seqlens=[5, 256, 255]),
+    "boosted_keys": dict(B=1, H_q=2, H_kv=2, N_q=1000, N_k=1000, d=128, causal=True,
+                         boost_frac=0.05, boost=3.0),
+    "negative_scale": dict(B=1, H_q=1, H_kv=1, N_q=256, N_k=256, d=64, scale=-0.2, causal=False),
+    "zero_scale": dict(B=1, H_q=1, H_kv=1, N_q=130, N_k=130, d=64, scale=0.0, causal=True),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_forward_backward(name):
+    kw = dict(SMALL[name])
+    inp = W.custom(seed=100 + len(name), **kw)
+    o, lse, dev = run_forward(inp)
+    _oracle_fwd_check(inp, o, lse, _all_pairs(inp))
+    dq, dk, dv = run_backward(inp, o, lse, dev)
+    _oracle_bwd_check(inp, dq, dk, dv, _all_groups(inp))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_worked_example_on_gpu(d):
+    """One query, 256 keys in two key tiles; only key 0 (score 0) and key 128
+    (score ln 3) matter, with values 2 and 10: O = 8 in every column. With scale
+    20 the running max jumps by far more than 2^8 across the tiles, which forces
+    the rescale branch."""
+    import torch
+    from exact_attention_15_gb300 import binding
+    for scale, expected in ((math.log(3.0), 8.0), (20.0, None)):
+        q = torch.zeros(1, 1, 1, d, dtype=torch.bfloat16, device="cuda")
+        q[..., 0] = 1.0
+        k = torch.zeros(1, 256, 1, d, dtype=torch.bfloat16, device="cuda")
+        k[0, :, 0, 0] = -64.0
+        k[0, 0, 0, 0] = 0.0
+        k[0, 128, 0, 0] = 1.0
+        v = torch.zeros(1, 256, 1, d, dtype=torch.bfloat16, device="cuda")
+        v[0, 0] = 2.0
+        v[0, 128] = 10.0
+        o, lse = binding.forward(q, k, v, scale=scale)
+        torch.cuda.synchronize()
+        o = o.float().cpu().numpy()[0, 0, 0]
+        if expected is None:
+            # weights e^0 : e^20 -> essentially all on key 128
+            w1 = 1.0 / (1.0 + math.exp(-20.0))
+            expected = 2.0 * (1 - w1) + 10.0 * w1
+        assert np.max(np.abs(o - expected)) < 3e-2, (scale, o[:4])
+        ref_lse = math.log(1.0 + math.exp(scale))
+        assert abs(float(lse.cpu()[0, 0, 0]) - ref_lse) < 2e-3
+
+
+def test_no_keys_and_empty_batch():
+    import torch
+    from exact_attention_15_gb300 import binding
+    q = torch.randn(1, 5, 2, 64, device="cuda").bfloat16()
+    k = torch.empty(1, 0, 2, 64, device="cuda", dtype=torch.bfloat16)
+    o, lse = binding.forward(q, k, k)
+    torch.cuda.synchronize()
+    assert torch.all(o == 0)
+    assert torch.all(torch.isinf(lse)) and torch.all(lse < 0)
+    q0 = torch.empty(0, 5, 2, 64, device="cuda", dtype=torch.bfloat16)
+    binding.forward(q0, q0, q0)
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+def _sample(rng, items, n):
+    idx = rng.choice(len(items), size=min(n, len(items)), replace=False)
+    return [items[i] for i in sorted(idx)]
+
+
+FULL = [
+    ("tiny", None, None),
+    ("short", 8, None),
+    ("short_causal", 8, None),
+    ("mid", 3, 512),
+    ("mid_causal", 3, 512),
+    ("long", 2, 384),
+    ("varlen_gqa", 2, None),
+]
+
+
+@pytest.mark.parametrize("name,n_pairs,n_rows", FULL, ids=[f[0] for f in FULL])
+def test_workload_forward(name, n_pairs, n_rows):
+    inp = W.generate(name, parts=("q", "k", "v"))
+    o, lse, _ = run_forward(inp)
+    rng = np.random.default_rng(7)
+    pairs = _all_pairs(inp) if n_pairs is None else _sample(rng, _all_pairs(inp), n_pairs)
+    rows = None if n_rows is None else np.sort(rng.choice(inp.N_q if inp.cu_seqlens is None else 512,
+                                                             size=n_rows, replace=False))
+    _oracle_fwd_check(inp, o, lse, pairs, rows)
+
+
+BWD_FULL = [("tiny", None), ("short", 3), ("short_causal", 3), ("mid", 1), ("mid_causal", 1),
+            ("long", 1), ("varlen_gqa", 1)]
+
+
+@pytest.mark.parametrize("name,n_groups", BWD_FULL, ids=[f[0] for f in BWD_FULL])
+def test_workload_backward(name, n_groups):
+    inp = W.generate(name)
+    o, lse, dev = run_forward(inp)
+    dq, dk, dv = run_backward(inp, o, lse, dev)
+    rng = np.random.default_rng(11)
+    groups = _all_groups(inp) if n_groups is None else _sample(rng, _all_groups(inp), n_groups)
+    _oracle_bwd_check(inp, dq, dk, dv, groups)
+
+
+@pytest.mark.parametrize("name", ["varlen_gqa", "short_causal"])
+def test_deterministic_backward(name):
+    """Deterministic mode: three runs bit-identical, and within tolerance."""
+    import torch
+    inp = W.generate(name)
+    o, lse, dev = run_forward(inp)
+    runs = [run_backward(inp, o, lse, dev, deterministic=True) for _ in range(3)]
+    for r in runs[1:]:
+        for a, b in zip(runs[0], r):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), "not bit-identical"
+    rng = np.random.default_rng(13)
+    _oracle_bwd_check(inp, *runs[0], _sample(rng, _all_groups(inp), 1))
