@@ -334,6 +334,9 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   if (!bwd_plan(B, H_q, H_kv, N_q, N_k, d, seqlens != nullptr, deterministic != 0, &pl))
     return ATTN_ERR_BAD_SHAPE;
   if (B == 0) return ATTN_OK;
+  const bool empty = (N_q == 0 || N_k == 0);
+  if (!empty && (workspace == nullptr || workspace_bytes < pl.total)) return ATTN_ERR_WORKSPACE;
+  if (!empty && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTN_ERR_ALIGNMENT;
   int dev;
   if ((st = current_device(&dev)) != ATTN_OK) return st;
   int* err = nullptr;
@@ -341,7 +344,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const size_t q_bytes = static_cast<size_t>(pl.rows_q) * H_q * d * 2;
   const size_t k_bytes = static_cast<size_t>(s.varlen ? N_k : static_cast<long long>(B) * N_k) * H_kv * d * 2;
-  if (N_q == 0 || N_k == 0) {
+  if (empty) {
     // no query rows: no key gradient; no keys: every row sees nothing
     if ((q_bytes && cudaMemsetAsync(dq, 0, q_bytes, cs) != cudaSuccess) ||
         (k_bytes && cudaMemsetAsync(dk, 0, k_bytes, cs) != cudaSuccess) ||
@@ -349,9 +352,6 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
       return ATTN_ERR_CUDA;
     return ATTN_OK;
   }
-  if (workspace == nullptr || workspace_bytes < pl.total) return ATTN_ERR_WORKSPACE;
-  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_ALIGNMENT;
-
   CUtensorMap maps[4];
   if (encode_rows_map(&maps[0], q, d, H_q, s.q_rows, s.q_batch) != ATTN_OK ||
       encode_rows_map(&maps[1], k, d, H_kv, s.k_rows, s.q_batch) != ATTN_OK ||
