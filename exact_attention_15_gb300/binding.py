@@ -33,6 +33,8 @@ _SIGS = {
     "attn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
                       ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
+    "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
+                              ctypes.c_float, _I, _P]),
     "attn_check": (_I, [_P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_debug_exp2": (_I, [_P, _P, _I, _I, _P]),
@@ -96,6 +98,17 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H_q, H_kv, N_q, N_k, d, causa
     return load().attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H_q, H_kv, N_q, N_k, d,
                            int(causal), seqlens, float(scale), int(deterministic), workspace,
                            workspace_bytes, stream)
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H_q, H_kv, N_q, N_k, d, causal,
+                     seqlens, scale, deterministic, stream) -> int:
+    """attn_bwd served from the library's own fixed scratch buffer (no workspace,
+    no allocation); for callers that cannot allocate device memory."""
+    return load().attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H_q, H_kv, N_q, N_k, d,
+                                   int(causal), seqlens, float(scale), int(deterministic), stream)
+
+
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 def attn_check(stream=None) -> int:

@@ -117,6 +117,37 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              void* workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * Size of the library's own scratch buffer used by attn_bwd_noalloc: 64 MiB on
+ * every GPU that loads the library, held until the process exits.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * attn_bwd without a workspace argument, for callers that cannot allocate device
+ * memory when they run the backward pass (a plugin whose host program owns all
+ * device memory through its own pool and offers no allocator; a latency-critical
+ * loop where cudaMalloc / cudaFree would stall on an implicit device
+ * synchronisation). The pages this library follows have no counterpart of this
+ * call: it is an interface convenience, not part of the method.
+ *
+ * Arguments, layouts, results and determinism are those of attn_bwd; inputs and
+ * outputs are still caller-owned. The scratch is a fixed
+ * ATTN_NOALLOC_SCRATCH_BYTES buffer inside the library's device code; nothing is
+ * allocated. Problems whose attn_bwd_workspace_bytes(...) exceeds that size are
+ * rejected with ATTN_ERR_WORKSPACE before anything is launched. The first call on
+ * a device looks up the buffer's device address for that device (with the
+ * device current); make that first call before any stream capture. All calls on
+ * a device share the one buffer and it keeps the last call's contents (the call
+ * clears what must start at zero), so calls whose kernels overlap on the GPU
+ * (different streams, or different host threads) race on it and give wrong
+ * results: serialise them.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dout, void* dq, void* dk, void* dv,
+                     int B, int H_q, int H_kv, int N_q, int N_k, int d, int causal,
+                     const int* seqlens, float scale, int deterministic, attn_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns ATTN_ERR_TIMEOUT if a kernel of this
  * library on the current device recorded a timed-out wait since the last check
  * (and clears the record), ATTN_ERR_CUDA if the stream reports an error, else
