@@ -38,6 +38,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the batch size (small cases for profiling)")
+    ap.add_argument("--causal", action="store_true", help="causal variant of the workload")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -203,8 +206,12 @@ def main():
         dist.init_process_group("nccl")
     binding.load()
 
-    w = W.WORKLOADS[WORKLOAD]
-    inp = W.generate(WORKLOAD)
+    w = W.WORKLOADS[WORKLOAD + ("_causal" if args.causal else "")]
+    if args.batch is not None:
+        inp = W.custom(args.batch, w.H_q, w.H_kv, w.N, w.N, w.d, w.scale, w.causal, seed=w.seed)
+        w = W.Workload(w.name, args.batch, w.H_q, w.H_kv, w.N, w.d, w.scale, w.causal, w.seed)
+    else:
+        inp = W.generate(w.name)
     dev = lambda bits: torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
     q, k, v, do = dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.do)
     B, H, N, d = w.B, w.H_q, w.N, w.d
@@ -328,7 +335,7 @@ def main():
             "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": f"{WORKLOAD}: B4 H16 N8192 d128 non-causal, scale 1/sqrt(128), fwd+bwd",
+            "config": {"workload": f"{w.name}: B{B} H{H} N{N} d{d} {'causal' if w.causal else 'non-causal'}, scale 1/sqrt(128), fwd+bwd",
                        "global_batch": B * world, "seq_len": N, "heads": H, "head_dim": d,
                        "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (q, k, v, o, dO: 128 MiB each)"},

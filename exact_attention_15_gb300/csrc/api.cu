@@ -82,16 +82,19 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // columns of one head, 128-byte swizzle (so the tile lands in shared memory in
 // the layout the tcgen05 descriptors expect).
 int encode_rows_map(CUtensorMap* m, const void* base, int d, int heads, long long rows,
-                    long long batch) {
+                    long long batch, bool fp32 = false) {
+  const cuuint64_t es_bytes = fp32 ? 4 : 2;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
                         static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(batch)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,
-                           static_cast<cuuint64_t>(d) * 2 * heads,
-                           static_cast<cuuint64_t>(d) * 2 * heads * rows};
-  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * es_bytes,
+                           static_cast<cuuint64_t>(d) * es_bytes * heads,
+                           static_cast<cuuint64_t>(d) * es_bytes * heads * rows};
+  // 128 bytes of the innermost dimension per box row: 64 bf16 or 32 fp32
+  cuuint32_t box[4] = {fp32 ? 32u : 64u, 1, 128, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
-                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = g_encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        4, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -352,14 +355,15 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
       return ATTN_ERR_CUDA;
     return ATTN_OK;
   }
-  CUtensorMap maps[4];
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  CUtensorMap maps[5];
   if (encode_rows_map(&maps[0], q, d, H_q, s.q_rows, s.q_batch) != ATTN_OK ||
       encode_rows_map(&maps[1], k, d, H_kv, s.k_rows, s.q_batch) != ATTN_OK ||
       encode_rows_map(&maps[2], v, d, H_kv, s.k_rows, s.q_batch) != ATTN_OK ||
-      encode_rows_map(&maps[3], dout, d, H_q, s.q_rows, s.q_batch) != ATTN_OK)
+      encode_rows_map(&maps[3], dout, d, H_q, s.q_rows, s.q_batch) != ATTN_OK ||
+      encode_rows_map(&maps[4], ws + pl.acc_off, d, H_q, s.q_rows, s.q_batch, true) != ATTN_OK)
     return ATTN_ERR_CUDA;
 
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
   BwdParams p;
   p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.dout = dout;
   p.dq = dq; p.dk = dk; p.dv = dv;

@@ -11,7 +11,7 @@
 //             dP^T = V dO_i^T       (SS)
 //             dV  += P^T dO_i       (TS, P^T from TMEM)
 //                                             dS^T = P^T o (dP^T - D_i)
-//             dK  += dS^T Q_i       (TS, dS^T from TMEM)
+//             dK  += dS^T Q_i       (SS, dS^T from shared memory)
 //             dQ_i = dS K           (SS, dS from shared memory)
 //         and adds dQ_i into the fp32 accumulator with vector reductions; in
 //         deterministic mode the additions into one query tile happen in
@@ -19,17 +19,20 @@
 //         (section 3.2.4).
 //   post  dQ = alpha * dQacc -> bf16.
 //
-// Warp roles of the main kernel (384 threads):
+// Warp roles of the main kernel (512 threads):
 //   warp 0      producer: Q_i and dO_i by TMA into a two-stage ring, LSE_i and D_i
 //               (plain loads) into the same stage.
 //   warp 1      TMEM owner and MMA issuer (one thread).
-//   warps 4-7   "compute": thread r owns key row r: P^T row, dS^T row, and at the
-//               end the dK / dV epilogue.
-//   warps 8-11  "dQ": thread r owns query row r of the dQ_i tile: TMEM -> registers
+//   warps 4-11  "compute", two warpgroups: thread r of warpgroup c owns key row r
+//               and query columns [64c, 64c+64): P^T, dS^T, and at the end half of
+//               the dK / dV row.
+//   warps 12-15 "dQ": thread r owns query row r of the dQ_i tile: TMEM -> registers
 //               -> fp32 reductions into the accumulator.
 //
-// TMEM (512 columns): dV [0, d), dK [d, 2d), S^T / P^T / dS^T [2d, 2d+128),
-// dP^T / dQ [2d+128, 2d+256).
+// TMEM (512 columns): dV [0, d), dK [d, 2d), S^T / P^T [2d, 2d+128),
+// dP^T / dQ [2d+128, 2d+256). dS lives only in shared memory: the same
+// 128-byte-swizzled buffer is the K-major A operand of dK = dS^T Q and the
+// MN-major A operand of dQ = dS K.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -43,9 +46,10 @@ struct BwdCfg {
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kTileBytes;
   static constexpr int kQOff = kVOff + kTileBytes;             // 2 stages
-  static constexpr int kdOOff = kQOff + 2 * kTileBytes;        // 2 stages
-  static constexpr int kdSOff = kdOOff + 2 * kTileBytes;       // 128 x 128 bf16
-  static constexpr int kStatOff = kdSOff + 128 * 128 * 2;      // per stage: lse2[128], D[128]
+  static constexpr int kdOOff = kQOff + 2 * kTileBytes;        // 1 stage (reloaded once dV is done)
+  static constexpr int kdSOff = kdOOff + kTileBytes;           // 128 x 128 bf16
+  static constexpr int kdQOff = kdSOff + 128 * 128 * 2;        // 2 x (128 rows x 32 fp32) staging
+  static constexpr int kStatOff = kdQOff + 2 * 16384;          // per Q stage: lse2[128], D[128]
   static constexpr int kBarOff = kStatOff + 2 * 2 * 128 * 4;
   static constexpr int kSmemBytes = kBarOff + 256;
   static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
@@ -54,8 +58,9 @@ struct BwdCfg {
 
 struct BwdBars {
   uint64_t kv_full;
-  uint64_t qdo_full[2];
-  uint64_t qdo_empty[2];
+  uint64_t q_full[2];   // Q_i, LSE_i and D_i of stage i % 2
+  uint64_t q_empty[2];
+  uint64_t do_full, do_empty;
   uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free;
   uint32_t tmem_base;
   int work_idx;
@@ -203,10 +208,10 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk16) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
 attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                     const BwdParams p, int* ticket) {
+                     const __grid_constant__ CUtensorMap tm_dq, const BwdParams p, int* ticket) {
   using Cfg = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + Cfg::kBarOff);
@@ -233,13 +238,15 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   if (tid == 0) {
     mbar_init(smem_addr(&bars->kv_full), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_addr(&bars->qdo_full[s]), 32);
-      mbar_init(smem_addr(&bars->qdo_empty[s]), 1);
+      mbar_init(smem_addr(&bars->q_full[s]), 32);
+      mbar_init(smem_addr(&bars->q_empty[s]), 1);
     }
+    mbar_init(smem_addr(&bars->do_full), 1);
+    mbar_init(smem_addr(&bars->do_empty), 1);
     mbar_init(smem_addr(&bars->s_full), 1);
     mbar_init(smem_addr(&bars->dp_full), 1);
-    mbar_init(smem_addr(&bars->p_ready), 128);
-    mbar_init(smem_addr(&bars->ds_ready), 128);
+    mbar_init(smem_addr(&bars->p_ready), 256);
+    mbar_init(smem_addr(&bars->ds_ready), 256);
     mbar_init(smem_addr(&bars->dq_full), 1);
     mbar_init(smem_addr(&bars->dq_free), 128);
     fence_barrier_init();
@@ -253,8 +260,10 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  // Register split: 128 x 72 (warps 0-3) + 256 x 136 (compute) + 128 x 160 (dQ)
+  // = 64,512 <= 512 x 128 (the launch total).
   if (warp < 4) {
-    regs_dec<56>();
+    regs_dec<72>();
     if (warp == 0) {
       // ------------------------------------------------------- producer
       if (n_it > 0) {
@@ -275,19 +284,16 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           const int stage = it & 1;
           const int h = t.h_kv * p.group + it / n_per_head;
           const int i = t.i_start + it % n_per_head;
-          if (!mbar_wait(smem_addr(&bars->qdo_empty[stage]), ((it >> 1) & 1) ^ 1, lim)) {
+          if (!mbar_wait(smem_addr(&bars->q_empty[stage]), ((it >> 1) & 1) ^ 1, lim)) {
             record_error(p.err, kErrTimeout);
             break;
           }
-          const uint32_t fb = smem_addr(&bars->qdo_full[stage]);
+          const uint32_t fb = smem_addr(&bars->q_full[stage]);
           if (lane == 0) {
-            mbar_expect_tx(fb, 2 * Cfg::kTileBytes);
-            for (int hf = 0; hf < D / 64; ++hf) {
+            mbar_expect_tx(fb, Cfg::kTileBytes);
+            for (int hf = 0; hf < D / 64; ++hf)
               tma_load_4d(smem_addr(smem + Cfg::kQOff + stage * Cfg::kTileBytes) + hf * 16384, &tm_q,
                           fb, hf * 64, h, t.row_base + i * kTileM, t.batch_coord);
-              tma_load_4d(smem_addr(smem + Cfg::kdOOff + stage * Cfg::kTileBytes) + hf * 16384,
-                          &tm_do, fb, hf * 64, h, t.row_base + i * kTileM, t.batch_coord);
-            }
           }
           // LSE (to log2 units) and D for the 128 rows of this query tile; rows
           // past the end get LSE = +inf so that their P is exactly 0.
@@ -310,153 +316,201 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             dvs[r] = dv;
           }
           mbar_arrive(fb);
+          // dO_i into the single dO buffer once dV_{i-1} has read it
+          if (!mbar_wait(smem_addr(&bars->do_empty), (it & 1) ^ 1, lim)) {
+            record_error(p.err, kErrTimeout);
+            break;
+          }
+          if (lane == 0) {
+            const uint32_t db = smem_addr(&bars->do_full);
+            mbar_arrive_expect_tx(db, Cfg::kTileBytes);
+            for (int hf = 0; hf < D / 64; ++hf)
+              tma_load_4d(smem_addr(smem + Cfg::kdOOff) + hf * 16384, &tm_do, db, hf * 64, h,
+                          t.row_base + i * kTileM, t.batch_coord);
+          }
+          __syncwarp();
         }
       }
     } else if (warp == 1) {
       // ------------------------------------------------------- MMA issuer
+      // Issue order per query tile i (S_{i+1} goes ahead of dK_i / dQ_i so the
+      // tensor core has work while the compute warps turn dP_i into dS_i and
+      // S_{i+1} into P_{i+1}):
+      //   S_0, dP_0 | dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1} | ...
       if (lane == 0 && n_it > 0) {
-        constexpr uint32_t kIdSS = make_idesc_bf16(128, 128, 0, 0);     // S^T, dP^T
-        constexpr uint32_t kIdTS = make_idesc_bf16(128, D, 0, 1);       // dV, dK
-        constexpr uint32_t kIdDQ = make_idesc_bf16(128, D, 1, 1);       // dQ
+        constexpr uint32_t kIdSS = make_idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
+        constexpr uint32_t kIdKM = make_idesc_bf16(128, D, 0, 1);    // dV, dK: B MN-major
+        constexpr uint32_t kIdDQ = make_idesc_bf16(128, D, 1, 1);    // dQ: A and B MN-major
         const uint32_t k_base = smem_addr(smem + Cfg::kKOff);
         const uint32_t v_base = smem_addr(smem + Cfg::kVOff);
         const uint32_t ds_base = smem_addr(smem + Cfg::kdSOff);
-        bool ok = mbar_wait(smem_addr(&bars->kv_full), 0, lim);
-        for (int it = 0; ok && it < n_it; ++it) {
-          const int stage = it & 1;
-          const uint32_t q_base = smem_addr(smem + Cfg::kQOff + stage * Cfg::kTileBytes);
-          const uint32_t do_base = smem_addr(smem + Cfg::kdOOff + stage * Cfg::kTileBytes);
-          if (!(ok = mbar_wait(smem_addr(&bars->qdo_full[stage]), (it >> 1) & 1, lim))) break;
-          tc_fence_after();
-          // S^T = K Q^T
+        auto q_base = [&](int it) { return smem_addr(smem + Cfg::kQOff + (it & 1) * Cfg::kTileBytes); };
+        auto do_base = [&](int) { return smem_addr(smem + Cfg::kdOOff); };
+        auto issue_s = [&](int it) {  // S^T = K Q^T
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
             mma_ss(tmem + Cfg::kColS, make_sdesc_sw128(k_base + off, 16, 1024),
-                   make_sdesc_sw128(q_base + off, 16, 1024), kIdSS, kk > 0);
+                   make_sdesc_sw128(q_base(it) + off, 16, 1024), kIdSS, kk > 0);
           }
           mma_commit(smem_addr(&bars->s_full));
-          // dP^T = V dO^T (its TMEM columns hold dQ_{it-1} until that is read out)
-          if (it > 0 && !(ok = mbar_wait(smem_addr(&bars->dq_free), (it - 1) & 1, lim))) break;
-          tc_fence_after();
+        };
+        auto issue_dp = [&](int it) {  // dP^T = V dO^T
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
             mma_ss(tmem + Cfg::kColDP, make_sdesc_sw128(v_base + off, 16, 1024),
-                   make_sdesc_sw128(do_base + off, 16, 1024), kIdSS, kk > 0);
+                   make_sdesc_sw128(do_base(it) + off, 16, 1024), kIdSS, kk > 0);
           }
           mma_commit(smem_addr(&bars->dp_full));
-          // dV += P^T dO
+        };
+        bool ok = mbar_wait(smem_addr(&bars->kv_full), 0, lim);
+        if (ok) ok = mbar_wait(smem_addr(&bars->q_full[0]), 0, lim);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+        }
+        if (ok) ok = mbar_wait(smem_addr(&bars->do_full), 0, lim);
+        if (ok) {
+          tc_fence_after();
+          issue_dp(0);
+        }
+        for (int it = 0; ok && it < n_it; ++it) {
+          const int stage = it & 1;
+          // dV += P^T dO  (P^T from TMEM)
           if (!(ok = mbar_wait(smem_addr(&bars->p_ready), it & 1, lim))) break;
           tc_fence_after();
+          // P^T for queries [0, 64) sits in S^T columns [0, 32), for queries
+          // [64, 128) in columns [64, 96); each MMA reads one 16-query slice
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk)
-            mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + kk * 8,
-                   make_sdesc_sw128(do_base + kk * 2048, 16384, 1024), kIdTS, (it > 0 || kk > 0));
-          // dK += dS^T Q ; dQ = dS K
+            mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
+                   make_sdesc_sw128(do_base(it) + kk * 2048, 16384, 1024), kIdKM, (it > 0 || kk > 0));
+          mma_commit(smem_addr(&bars->do_empty));  // dO_i fully read: the next one may load
+          // S^T of the next query tile into the same TMEM columns (the MMAs run
+          // in issue order, so dV has read P^T before they are overwritten)
+          if (it + 1 < n_it) {
+            if (!(ok = mbar_wait(smem_addr(&bars->q_full[(it + 1) & 1]), ((it + 1) >> 1) & 1, lim))) break;
+            tc_fence_after();
+            issue_s(it + 1);
+          }
+          // dK += dS^T Q (dS^T: the shared-memory dS buffer read K-major);
+          // dQ = dS K (the same buffer read MN-major)
           if (!(ok = mbar_wait(smem_addr(&bars->ds_ready), it & 1, lim))) break;
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kTileM / 16; ++kk)
-            mma_ts(tmem + Cfg::kColDK, tmem + Cfg::kColS + 64 + kk * 8,
-                   make_sdesc_sw128(q_base + kk * 2048, 16384, 1024), kIdTS, (it > 0 || kk > 0));
+          for (int kk = 0; kk < kTileM / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_ss(tmem + Cfg::kColDK, make_sdesc_sw128(ds_base + off, 16, 1024),
+                   make_sdesc_sw128(q_base(it) + kk * 2048, 16384, 1024), kIdKM, (it > 0 || kk > 0));
+          }
 #pragma unroll
           for (int kk = 0; kk < kTileN / 16; ++kk)
             mma_ss(tmem + Cfg::kColDP, make_sdesc_sw128(ds_base + kk * 2048, 16384, 1024),
                    make_sdesc_sw128(k_base + kk * 2048, 16384, 1024), kIdDQ, kk > 0);
           mma_commit(smem_addr(&bars->dq_full));
-          mma_commit(smem_addr(&bars->qdo_empty[stage]));
+          mma_commit(smem_addr(&bars->q_empty[stage]));
+          // dP^T of the next tile reuses the dQ columns once dQ_i has been read out
+          if (it + 1 < n_it) {
+            if (!(ok = mbar_wait(smem_addr(&bars->dq_free), it & 1, lim))) break;
+            if (!(ok = mbar_wait(smem_addr(&bars->do_full), (it + 1) & 1, lim))) break;
+            tc_fence_after();
+            issue_dp(it + 1);
+          }
         }
         if (!ok) record_error(p.err, kErrTimeout);
       }
     }
     __syncwarp();
-  } else if (warp < 8) {
-    regs_inc<224>();
-    // --------------------------------------------------------- compute (key row r)
-    const int r = tid - 128;
+  } else if (warp < 12) {
+    regs_inc<136>();
+    // --------------------------------------------------------- compute
+    // Thread (warpgroup c, lane row r) owns key row r and query columns
+    // [64c, 64c + 64) of S^T, P^T, dP^T and dS^T.
+    const int c = (warp - 4) >> 2;
+    const int r = (tid - 128) & 127;
     const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
     const int kv = t.j * kTileN + r;       // sequence-relative key row
     const bool kv_ok = kv < t.Lk;
-    const float c = p.scale_log2;
+    const float sc = p.scale_log2;
     const float* stat = reinterpret_cast<const float*>(smem + Cfg::kStatOff);
-    uint8_t* ds_smem = smem + Cfg::kdSOff;
+    uint8_t* ds_blk = smem + Cfg::kdSOff + c * 16384;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int stage = it & 1;
       const int i = t.i_start + it % n_per_head;
-      if (!(ok = mbar_wait(smem_addr(&bars->qdo_full[stage]), (it >> 1) & 1, lim))) break;
+      if (!(ok = mbar_wait(smem_addr(&bars->q_full[stage]), (it >> 1) & 1, lim))) break;
       if (!(ok = mbar_wait(smem_addr(&bars->s_full), it & 1, lim))) break;
       tc_fence_after();
-      const float* lse2 = stat + stage * 256;
-      const float* dvs = lse2 + 128;
-      float pr[128];
+      const float* lse2 = stat + stage * 256 + 64 * c;
+      const float* dvs = stat + stage * 256 + 128 + 64 * c;
+      float pr[64];
       {
-        uint32_t sr[128];
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-          tmem_ld32(tmem + lane_base + Cfg::kColS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + cc * 32));
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + cc * 32));
+        uint32_t sr[64];
+        tmem_ld32(tmem + lane_base + Cfg::kColS + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld32(tmem + lane_base + Cfg::kColS + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + 32));
         const bool diag = p.causal && (i == t.j);
 #pragma unroll
-        for (int q = 0; q < 128; q += 4) {
+        for (int q = 0; q < 64; q += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(lse2 + q);
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            float pv = ex2_approx(fmaf(__uint_as_float(sr[q + e]), c, -lv[e]));
-            if (diag && (r > q + e)) pv = 0.f;  // key after query: masked
+            float pv = ex2_approx(fmaf(__uint_as_float(sr[q + e]), sc, -lv[e]));
+            if (diag && (r > 64 * c + q + e)) pv = 0.f;  // key after query: masked
             pr[q + e] = kv_ok ? pv : 0.f;
           }
         }
       }
       {
-        uint32_t pk[64];
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 64; ++e) pk[e] = pack_bf16x2(pr[2 * e], pr[2 * e + 1]);
-        tmem_st32(tmem + lane_base + Cfg::kColS, *reinterpret_cast<uint32_t(*)[32]>(pk));
-        tmem_st32(tmem + lane_base + Cfg::kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(pr[2 * e], pr[2 * e + 1]);
+        // P^T (bf16 pairs) for query columns [64c, 64c+64) goes into the first
+        // 32 of this warpgroup's own 64 S^T columns, so it never overwrites scores
+        // the other warpgroup has still to read.
+        tmem_st32(tmem + lane_base + Cfg::kColS + 64 * c, pk);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_addr(&bars->p_ready));
       // dS^T = P^T o (dP^T - D)
       if (!(ok = mbar_wait(smem_addr(&bars->dp_full), it & 1, lim))) break;
-      // the previous dQ MMA read dS from shared memory; it must have finished
+      // dK_{i-1} and dQ_{i-1} read dS from shared memory; they must have finished
       if (it > 0 && !(ok = mbar_wait(smem_addr(&bars->dq_full), (it - 1) & 1, lim))) break;
       tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t dp[32];
-        tmem_ld32(tmem + lane_base + Cfg::kColDP + cc * 32, dp);
+        tmem_ld32(tmem + lane_base + Cfg::kColDP + 64 * c + 32 * cc, dp);
         tmem_ld_wait(dp);
         uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int q0 = cc * 32 + 2 * e;
-          const float d0 = pr[q0] * (__uint_as_float(dp[2 * e]) - dvs[q0]);
-          const float d1 = pr[q0 + 1] * (__uint_as_float(dp[2 * e + 1]) - dvs[q0 + 1]);
-          w[e] = pack_bf16x2(d0, d1);
+        for (int e = 0; e < 8; ++e) {
+          const int q0 = 32 * cc + 4 * e;
+          const float4 d4 = *reinterpret_cast<const float4*>(dvs + q0);
+          w[2 * e] = pack_bf16x2(pr[q0] * (__uint_as_float(dp[4 * e]) - d4.x),
+                                 pr[q0 + 1] * (__uint_as_float(dp[4 * e + 1]) - d4.y));
+          w[2 * e + 1] = pack_bf16x2(pr[q0 + 2] * (__uint_as_float(dp[4 * e + 2]) - d4.z),
+                                     pr[q0 + 3] * (__uint_as_float(dp[4 * e + 3]) - d4.w));
         }
-        tmem_st16(tmem + lane_base + Cfg::kColS + 64 + cc * 16, w);
-        // dS in shared memory as the MN-major A operand of dQ = dS K:
-        // block (cc / 2) holds query columns 64 * (cc / 2) ..; row r = key row.
-        uint8_t* blk = ds_smem + (cc >> 1) * 16384;
+        // dS (row r = key, 64 query columns of block c) in 128-byte-swizzled form:
+        // read MN-major it is the A operand of dQ = dS K, read K-major the A
+        // operand of dK = dS^T Q.
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          const int chunk = (cc & 1) * 4 + ch;  // 16-byte chunk (8 queries) within the 128-byte row
-          *reinterpret_cast<uint4*>(blk + sw128_offset(r, chunk)) =
+        for (int ch = 0; ch < 4; ++ch)
+          *reinterpret_cast<uint4*>(ds_blk + sw128_offset(r, cc * 4 + ch)) =
               make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
-        }
       }
-      tmem_st_wait();
       fence_async_shared();
       tc_fence_before();
       mbar_arrive(smem_addr(&bars->ds_ready));
     }
     if (!ok) record_error(p.err, kErrTimeout);
     // --------------------------------------------------------- dK / dV epilogue
+    // warpgroup c writes columns [c d/2, (c+1) d/2) of this key row
     bool have = ok && n_it > 0;
     if (have) {
       have = mbar_wait(smem_addr(&bars->dq_full), (n_it - 1) & 1, lim);
@@ -478,10 +532,11 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const float mul = which ? p.scale : 1.0f;
         uint4* dst = which ? dk_row : dv_row;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < D / 64; ++cc) {
+          const int c0 = c * (D / 2) + cc * 32;
           uint32_t v[32];
           if (have) {
-            tmem_ld32(tmem + lane_base + col + cc * 32, v);
+            tmem_ld32(tmem + lane_base + col + c0, v);
             tmem_ld_wait(v);
           } else {
 #pragma unroll
@@ -490,7 +545,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           if (kv_ok) {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              dst[cc * 4 + e] = make_uint4(
+              dst[c0 / 8 + e] = make_uint4(
                   pack_bf16x2(__uint_as_float(v[8 * e + 0]) * mul, __uint_as_float(v[8 * e + 1]) * mul),
                   pack_bf16x2(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul),
                   pack_bf16x2(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul),
@@ -500,9 +555,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       }
     }
   } else {
-    regs_inc<224>();
+    regs_inc<160>();
     // --------------------------------------------------------- dQ (query row r)
-    const int r = tid - 256;
+    const int r = tid - 384;
     const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
@@ -510,7 +565,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       const int i = t.i_start + it % n_per_head;
       if (!(ok = mbar_wait(smem_addr(&bars->dq_full), it & 1, lim))) break;
       tc_fence_after();
-      uint32_t v[128];
+      uint32_t v[D];
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc)
         tmem_ld32(tmem + lane_base + Cfg::kColDP + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(v + cc * 32));
@@ -518,7 +573,6 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       for (int cc = 0; cc < D / 32; ++cc) tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + cc * 32));
       tc_fence_before();
       mbar_arrive(smem_addr(&bars->dq_free));
-      const int q = i * kTileM + r;
       int* sem = nullptr;
       if (p.deterministic) {
         // wait until every key tile before this one has added into query tile i
@@ -531,22 +585,52 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
         named_bar_sync(1, 128);
       }
-      if (q < t.Lq) {
-        const size_t grow = static_cast<size_t>(t.row_base) + q;
-        const size_t off = p.cu_seqlens ? (grow * p.H_q + h) * D
-                                        : ((static_cast<size_t>(t.b) * p.N_q + q) * p.H_q + h) * D;
-        float* dst = p.dq_acc + off;
+      if (p.cu_seqlens != nullptr && (i + 1) * kTileM > t.Lq) {
+        // last tile of a packed sequence: a 128-row bulk reduction would also
+        // touch the next sequence's rows, so add the valid rows one by one
+        const int q = i * kTileM + r;
+        if (q < t.Lq) {
+          float* dst = p.dq_acc + ((static_cast<size_t>(t.row_base) + q) * p.H_q + h) * D;
 #pragma unroll
-        for (int e = 0; e < D / 4; ++e)
-          red_add_v4(dst + 4 * e, __uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                     __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+          for (int e = 0; e < D / 4; ++e)
+            red_add_v4(dst + 4 * e, __uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                       __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+        }
+      } else {
+        // 32 fp32 columns at a time: registers -> swizzled staging buffer ->
+        // one bulk tensor reduction (rows past the end of a fixed-length batch
+        // entry fall outside the tensor map and are dropped)
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          const int buf = cc & 1;
+          uint8_t* stage_buf = smem + Cfg::kdQOff + buf * 16384;
+          if (r == 0) bulk_wait_group_read<1>();  // this buffer's previous reduction has read it
+          named_bar_sync(1, 128);
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4*>(stage_buf + sw128_offset(r, ch)) =
+                make_uint4(v[cc * 32 + 4 * ch], v[cc * 32 + 4 * ch + 1], v[cc * 32 + 4 * ch + 2],
+                           v[cc * 32 + 4 * ch + 3]);
+          fence_async_shared();
+          named_bar_sync(1, 128);
+          if (r == 0) {
+            tma_reduce_add_4d(&tm_dq, smem_addr(stage_buf), cc * 32, h, t.row_base + i * kTileM,
+                              t.batch_coord);
+            bulk_commit_group();
+          }
+        }
       }
       if (p.deterministic) {
+        if (r == 0) {
+          bulk_wait_group<0>();  // our reductions are complete in global memory
+          fence_async_global();
+        }
         __threadfence();
         named_bar_sync(1, 128);
         if (r == 0) atomicAdd(sem, 1);
       }
     }
+    if (r == 0) bulk_wait_group<0>();  // staging buffers are read before the CTA exits
     if (!ok) record_error(p.err, kErrTimeout);
   }
   tc_fence_before();
@@ -579,7 +663,8 @@ static cudaError_t launch_bwd_impl(const BwdParams& p, const CUtensorMap* maps, 
     if (e != cudaSuccess) return e;
     int* ticket = p.deterministic ? p.sem + n_sem : nullptr;
     slot = prof_begin(kKBwdMain, st);
-    kern<<<n_work, 384, Cfg::kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3], p, ticket);
+    kern<<<n_work, 512, Cfg::kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p,
+                                               ticket);
     e = cudaGetLastError();
     prof_end(slot, st);
     if (e != cudaSuccess) return e;
