@@ -38,6 +38,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="named workload (tiny, short, short_causal, mid, mid_causal, long, varlen_gqa)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the batch size (small cases for profiling)")
     ap.add_argument("--causal", action="store_true", help="causal variant of the workload")
@@ -51,6 +53,23 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def max_over_ranks(x: float, world: int, device="cuda") -> float:
+    """Largest value of x over all ranks (the slowest rank decides the time)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(step_flops_per_rank: float, steps: int, world: int, max_ms: float) -> float:
+    """Weak scaling: every rank runs its own replica of the workload; the job's
+    throughput is all ranks' work over the slowest rank's time (TFLOP/s)."""
+    return world * step_flops_per_rank * steps / (max_ms * 1e-3) / 1e12
 
 
 def measured_peaks():
@@ -206,33 +225,42 @@ def main():
         dist.init_process_group("nccl")
     binding.load()
 
-    w = W.WORKLOADS[WORKLOAD + ("_causal" if args.causal else "")]
-    if args.batch is not None:
-        inp = W.custom(args.batch, w.H_q, w.H_kv, w.N, w.N, w.d, w.scale, w.causal, seed=w.seed)
+    name = args.workload
+    if args.causal and not name.endswith("_causal") and name + "_causal" in W.WORKLOADS:
+        name += "_causal"
+    w = W.WORKLOADS[name]
+    if args.batch is not None and w.varlen is None:
+        inp = W.custom(args.batch, w.H_q, w.H_kv, w.N, w.N, w.d, w.scale, w.causal, seed=w.seed,
+                       boost_frac=w.boost_frac, boost=w.boost)
         w = W.Workload(w.name, args.batch, w.H_q, w.H_kv, w.N, w.d, w.scale, w.causal, w.seed)
     else:
         inp = W.generate(w.name)
     dev = lambda bits: torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
     q, k, v, do = dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.do)
-    B, H, N, d = w.B, w.H_q, w.N, w.d
+    varlen = inp.cu_seqlens is not None
+    B, H, H_kv, d = inp.B, inp.H_q, inp.H_kv, inp.d
+    N = inp.N_q
+    cu = torch.from_numpy(inp.cu_seqlens).cuda() if varlen else None
+    cu_ptr = cu.data_ptr() if varlen else None
     o = torch.empty_like(q)
-    lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    lse = torch.empty((H, N) if varlen else (B, H, N), dtype=torch.float32, device="cuda")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws_bytes = binding.attn_bwd_workspace_bytes(B, H, H, N, N, d, 0, 0)
+    ws_bytes = binding.attn_bwd_workspace_bytes(B, H, H_kv, N, N, d, varlen, 0)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
 
     def step():
         st = binding.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                              B, H, H, N, N, d, w.causal, None, w.scale, sp)
+                              B, H, H_kv, N, N, d, w.causal, cu_ptr, w.scale, sp)
         assert st == 0, st
         st = binding.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                               do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                              B, H, H, N, N, d, w.causal, None, w.scale, 0, ws.data_ptr(), ws_bytes, sp)
+                              B, H, H_kv, N, N, d, w.causal, cu_ptr, w.scale, 0, ws.data_ptr(),
+                              ws_bytes, sp)
         assert st == 0, st
 
-    fwd_flops = W.fwd_flops(B, H, N, N, d, w.causal)
+    fwd_flops = W.fwd_flops(B, H, N, N, d, w.causal, seqlens=inp.seqlens() if varlen else None)
     step_flops = fwd_flops * 3.5  # forward + 2.5x backward
 
     for _ in range(max(args.warmup, 3)):
@@ -257,15 +285,12 @@ def main():
     clocks = sampler.stop()
     binding.attn_profile_enable(False)
     recs = binding.attn_profile_read()
-    ms_total = ev0.elapsed_time(ev1)
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world)
     if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
         torch.distributed.barrier()
     assert binding.attn_check(sp) == 0
     ms_step = ms_total / args.steps
-    value = world * step_flops * args.steps / (ms_total * 1e-3) / 1e12
+    value = whole_job_value(step_flops, args.steps, world, ms_total)
 
     per_kernel = {}
     for name, ms in recs:
@@ -318,12 +343,8 @@ def main():
             e2e_step()
         ev1.record(stream)
         torch.cuda.synchronize()
-        ms_e2e = ev0.elapsed_time(ev1)
-        if world > 1:
-            t = torch.tensor([ms_e2e], device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = {"value": world * step_flops * args.steps / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+        ms_e2e = max_over_ranks(ev0.elapsed_time(ev1), world)
+        e2e = {"value": whole_job_value(step_flops, args.steps, world, ms_e2e), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": ms_e2e / args.steps}
 
@@ -335,10 +356,12 @@ def main():
             "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": f"{w.name}: B{B} H{H} N{N} d{d} {'causal' if w.causal else 'non-causal'}, scale 1/sqrt(128), fwd+bwd",
-                       "global_batch": B * world, "seq_len": N, "heads": H, "head_dim": d,
+            "config": {"workload": f"{w.name}: " + (w.note or f"B{B} H{H} N{N} d{d}") + ", fwd+bwd",
+                       "global_batch": B * world, "seq_len": N, "heads": H, "kv_heads": H_kv,
+                       "head_dim": d,
                        "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2 (q, k, v, o, dO: 128 MiB each)"},
+                       "l2": f"inputs larger than L2 (q, k, v, o, dO: {q.numel() * 2 / 2**20:.0f} MiB each)"
+                             if q.numel() * 2 * 5 > 129e6 else "inputs smaller than L2 (L2 not flushed)"},
             "fwd_tflops": (fwd_flops / (fwd_ms * 1e-3) / 1e12) if fwd_ms else None,
             "kernels": kt,
             "roofline": roofline,

@@ -39,12 +39,16 @@ _SIGS = {
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_debug_exp2": (_I, [_P, _P, _I, _I, _P]),
     "attn_set_wait_limit": (ctypes.c_longlong, [ctypes.c_longlong]),
+    "attn_debug_inject": (_I, [_I]),
+    "attn_debug_stall": (_I, [_P]),
     "attn_profile_enable": (_I, [_I]),
     "attn_profile_read": (_I, [_P, _I]),
 }
 
 KERNEL_NAMES = {1: "attn_fwd_kernel", 2: "attn_bwd_pre_kernel", 3: "attn_bwd_main_kernel",
-                4: "attn_bwd_post_kernel", 5: "exp2_probe_kernel"}
+                4: "attn_bwd_post_kernel", 5: "exp2_probe_kernel", 6: "stall_probe_kernel"}
+FAULT_NONE = 0
+FAULT_SKIP_DQ_RELEASE = 1
 
 
 class ProfileRecord(ctypes.Structure):
@@ -124,6 +128,14 @@ attn_status_string = status_string
 
 def attn_debug_exp2(x, y, n, mode, stream) -> int:
     return load().attn_debug_exp2(x, y, n, mode, stream)
+
+
+def attn_debug_inject(fault: int) -> int:
+    return load().attn_debug_inject(int(fault))
+
+
+def attn_debug_stall(stream=None) -> int:
+    return load().attn_debug_stall(stream)
 
 
 def attn_set_wait_limit(cycles: int) -> int:

@@ -21,6 +21,7 @@ cudaError_t launch_attn_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const FwdParams& p, dim3 grid,
                             cudaStream_t stream);
 cudaError_t launch_exp2_probe(const float* x, float* y, int n, int mode, cudaStream_t stream);
+cudaError_t launch_stall_probe(int* err, long long limit, cudaStream_t stream);
 cudaError_t launch_attn_bwd(const BwdParams& p, const CUtensorMap* maps, cudaStream_t stream,
                             long long rows_q, int n_sem, int n_work);
 }  // namespace attn
@@ -37,6 +38,7 @@ std::mutex g_mu;
 int* g_err_ptr[kMaxDevices] = {};
 int g_dev_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 unsupported
 long long g_wait_limit = 2000000000ll;  // about one second of SM clock
+int g_fault = 0;                        // host-injected fault, see attn_debug_inject
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int current_device(int* dev) {
@@ -380,6 +382,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.scale_log2 = scale * kLog2e;
   p.err = err;
   p.wait_limit = g_wait_limit;
+  p.fault = g_fault;
   const int n_sem = static_cast<int>(pl.slots * H_q);
   if (launch_attn_bwd(p, maps, cs, pl.rows_q, n_sem, static_cast<int>(pl.n_work)) != cudaSuccess)
     return ATTN_ERR_CUDA;
@@ -403,6 +406,25 @@ int attn_check(attn_stream_t stream) {
     return ATTN_ERR_TIMEOUT;
   }
   return ATTN_OK;
+}
+
+int attn_debug_inject(int fault) {
+  if (fault != ATTN_FAULT_NONE && fault != ATTN_FAULT_SKIP_DQ_RELEASE) return ATTN_ERR_BAD_SHAPE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_fault = fault;
+  return ATTN_OK;
+}
+
+int attn_debug_stall(attn_stream_t stream) {
+  int dev;
+  int st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  int* err;
+  if ((st = device_setup(dev, &err)) != ATTN_OK) return st;
+  return launch_stall_probe(err, g_wait_limit, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_CUDA;
 }
 
 int attn_debug_exp2(const float* x, float* y, int n, int mode, attn_stream_t stream) {

@@ -21,6 +21,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTau = 8.0f;
 
 enum DevErr : int { kErrNone = 0, kErrTimeout = 1 };
+// Host-injected faults (attn_debug_inject); none of them can fault or hang the GPU.
+enum Fault : int { kFaultNone = 0, kFaultSkipDqRelease = 1 };
 
 struct FwdParams {
   void* o;              // bf16
@@ -49,11 +51,13 @@ struct BwdParams {
   float scale, scale_log2;
   int* err;
   long long wait_limit;
+  int fault;            // host-injected fault for failure tests (0 = none)
 };
 
 // Kernel tracing (host side, implemented next to the C ABI). prof_begin
 // returns a slot (or -1 when tracing is off); prof_end closes it.
-enum KernelId : int { kKFwd = 1, kKBwdPre = 2, kKBwdMain = 3, kKBwdPost = 4, kKExp2 = 5 };
+enum KernelId : int { kKFwd = 1, kKBwdPre = 2, kKBwdMain = 3, kKBwdPost = 4, kKExp2 = 5,
+                      kKStall = 6 };
 int prof_begin(int kernel, cudaStream_t stream);
 void prof_end(int slot, cudaStream_t stream);
 

@@ -455,6 +455,29 @@ __global__ void exp2_probe_kernel(const float* __restrict__ x, float* __restrict
   if (i < n) y[i] = mode ? exp2_poly3(x[i]) : ex2_approx(x[i]);
 }
 
+// Failure test: one CTA waits on an mbarrier that nothing ever arrives at. The
+// bounded wait gives up after `limit` cycles and records a timeout; nothing
+// else is in flight, so the kernel just returns.
+__global__ void stall_probe_kernel(int* err, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (!mbar_wait(smem_addr(&bar), 0, limit)) {
+    if (threadIdx.x == 0) record_error(err, kErrTimeout);
+  }
+}
+
+cudaError_t launch_stall_probe(int* err, long long limit, cudaStream_t stream) {
+  const int slot = prof_begin(kKStall, stream);
+  stall_probe_kernel<<<1, 32, 0, stream>>>(err, limit);
+  const cudaError_t e = cudaGetLastError();
+  prof_end(slot, stream);
+  return e;
+}
+
 cudaError_t launch_exp2_probe(const float* x, float* y, int n, int mode, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
   const int slot = prof_begin(kKExp2, stream);

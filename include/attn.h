@@ -167,6 +167,26 @@ const char* attn_status_string(int status);
 int attn_debug_exp2(const float* x, float* y, int n, int mode, attn_stream_t stream);
 
 /*
+ * Failure-path test hooks. They exercise the bounded device-side waits without
+ * faulting, trapping or hanging the GPU.
+ *
+ * attn_debug_inject(fault) sets a process-wide injected fault for later
+ * launches: ATTN_FAULT_NONE restores normal operation; ATTN_FAULT_SKIP_DQ_RELEASE
+ * makes the first work item of a deterministic attn_bwd never release its dQ
+ * ordering semaphores, so the key tiles after it give up waiting once the wait
+ * limit is spent and the call ends with ATTN_ERR_TIMEOUT recorded (its gradients
+ * are then not valid). Returns ATTN_ERR_BAD_SHAPE for an unknown fault.
+ *
+ * attn_debug_stall(stream) launches one CTA that waits on an mbarrier nothing
+ * arrives at; the wait gives up after the wait limit and records
+ * ATTN_ERR_TIMEOUT, which attn_check() then reports.
+ */
+#define ATTN_FAULT_NONE 0
+#define ATTN_FAULT_SKIP_DQ_RELEASE 1
+int attn_debug_inject(int fault);
+int attn_debug_stall(attn_stream_t stream);
+
+/*
  * Sets the cycle budget of every bounded device-side wait for later launches
  * on this process (default about one second of SM clock). Returns the old value.
  */
@@ -179,7 +199,7 @@ long long attn_set_wait_limit(long long cycles);
  * `max_records` records (oldest first) and discards everything it has read;
  * it returns the number of records written, or a negative attn_status.
  * Kernel ids: 1 forward, 2 backward pre (D, zeroing), 3 backward main,
- * 4 backward post (dQ conversion), 5 exp2 test hook.
+ * 4 backward post (dQ conversion), 5 exp2 test hook, 6 stall test hook.
  */
 typedef struct {
   int kernel;  /* kernel id, see above */
