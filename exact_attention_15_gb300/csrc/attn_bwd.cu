@@ -260,10 +260,10 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  // Register split: 128 x 72 (warps 0-3) + 256 x 136 (compute) + 128 x 160 (dQ)
+  // Register split: 128 x 104 (warps 0-3) + 256 x 128 (compute) + 128 x 144 (dQ)
   // = 64,512 <= 512 x 128 (the launch total).
   if (warp < 4) {
-    regs_dec<72>();
+    regs_dec<104>();
     if (warp == 0) {
       // ------------------------------------------------------- producer
       if (n_it > 0) {
@@ -341,27 +341,36 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         constexpr uint32_t kIdSS = make_idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
         constexpr uint32_t kIdKM = make_idesc_bf16(128, D, 0, 1);    // dV, dK: B MN-major
         constexpr uint32_t kIdDQ = make_idesc_bf16(128, D, 1, 1);    // dQ: A and B MN-major
+        // Descriptors are built once; each MMA only adds a compile-time byte
+        // offset (>> 4) to the start-address field, which keeps the single
+        // issuing thread ahead of the tensor core. Every tile is a
+        // 128-byte-swizzled [rows x 64] block pair that reads as K-major (lbo
+        // unused) or MN-major (lbo = 16 KB between the 64-column blocks).
         const uint32_t k_base = smem_addr(smem + Cfg::kKOff);
         const uint32_t v_base = smem_addr(smem + Cfg::kVOff);
         const uint32_t ds_base = smem_addr(smem + Cfg::kdSOff);
-        auto q_base = [&](int it) { return smem_addr(smem + Cfg::kQOff + (it & 1) * Cfg::kTileBytes); };
-        auto do_base = [&](int) { return smem_addr(smem + Cfg::kdOOff); };
+        const uint64_t k_km = make_sdesc_sw128(k_base, 16, 1024);
+        const uint64_t k_mn = make_sdesc_sw128(k_base, 16384, 1024);
+        const uint64_t v_km = make_sdesc_sw128(v_base, 16, 1024);
+        const uint64_t q_km = make_sdesc_sw128(smem_addr(smem + Cfg::kQOff), 16, 1024);
+        const uint64_t q_mn = make_sdesc_sw128(smem_addr(smem + Cfg::kQOff), 16384, 1024);
+        const uint64_t do_km = make_sdesc_sw128(smem_addr(smem + Cfg::kdOOff), 16, 1024);
+        const uint64_t do_mn = make_sdesc_sw128(smem_addr(smem + Cfg::kdOOff), 16384, 1024);
+        const uint64_t ds_km = make_sdesc_sw128(ds_base, 16, 1024);
+        const uint64_t ds_mn = make_sdesc_sw128(ds_base, 16384, 1024);
+        constexpr uint32_t kStageStep = Cfg::kTileBytes >> 4;
+        auto koff = [](int kk) { return static_cast<uint32_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4); };
         auto issue_s = [&](int it) {  // S^T = K Q^T
+          const uint64_t qb = q_km + (it & 1) * kStageStep;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tmem + Cfg::kColS, make_sdesc_sw128(k_base + off, 16, 1024),
-                   make_sdesc_sw128(q_base(it) + off, 16, 1024), kIdSS, kk > 0);
-          }
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + Cfg::kColS, k_km + koff(kk), qb + koff(kk), kIdSS, kk > 0);
           mma_commit(smem_addr(&bars->s_full));
         };
-        auto issue_dp = [&](int it) {  // dP^T = V dO^T
+        auto issue_dp = [&](int) {  // dP^T = V dO^T
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tmem + Cfg::kColDP, make_sdesc_sw128(v_base + off, 16, 1024),
-                   make_sdesc_sw128(do_base(it) + off, 16, 1024), kIdSS, kk > 0);
-          }
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + Cfg::kColDP, v_km + koff(kk), do_km + koff(kk), kIdSS, kk > 0);
           mma_commit(smem_addr(&bars->dp_full));
         };
         bool ok = mbar_wait(smem_addr(&bars->kv_full), 0, lim);
@@ -385,7 +394,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk)
             mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
-                   make_sdesc_sw128(do_base(it) + kk * 2048, 16384, 1024), kIdKM, (it > 0 || kk > 0));
+                   do_mn + kk * (2048 >> 4), kIdKM, (it > 0 || kk > 0));
           mma_commit(smem_addr(&bars->do_empty));  // dO_i fully read: the next one may load
           // S^T of the next query tile into the same TMEM columns (the MMAs run
           // in issue order, so dV has read P^T before they are overwritten)
@@ -398,17 +407,16 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           // dQ = dS K (the same buffer read MN-major)
           if (!(ok = mbar_wait(smem_addr(&bars->ds_ready), it & 1, lim))) break;
           tc_fence_after();
+          const uint64_t qmn = q_mn + (it & 1) * kStageStep;
 #pragma unroll
-          for (int kk = 0; kk < kTileM / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(tmem + Cfg::kColDK, make_sdesc_sw128(ds_base + off, 16, 1024),
-                   make_sdesc_sw128(q_base(it) + kk * 2048, 16384, 1024), kIdKM, (it > 0 || kk > 0));
-          }
+          for (int kk = 0; kk < kTileM / 16; ++kk)
+            mma_ss(tmem + Cfg::kColDK, ds_km + koff(kk), qmn + kk * (2048 >> 4), kIdKM,
+                   (it > 0 || kk > 0));
 #pragma unroll
           for (int kk = 0; kk < kTileN / 16; ++kk)
-            mma_ss(tmem + Cfg::kColDP, make_sdesc_sw128(ds_base + kk * 2048, 16384, 1024),
-                   make_sdesc_sw128(k_base + kk * 2048, 16384, 1024), kIdDQ, kk > 0);
-          mma_commit(smem_addr(&bars->dq_full));
+            mma_ss(tmem + Cfg::kColDP, ds_mn + kk * (2048 >> 4), k_mn + kk * (2048 >> 4), kIdDQ,
+                   kk > 0);
+          mma_commit(smem_addr(&bars->dq_full));  // covers every earlier MMA, dV included
           mma_commit(smem_addr(&bars->q_empty[stage]));
           // dP^T of the next tile reuses the dQ columns once dQ_i has been read out
           if (it + 1 < n_it) {
@@ -423,7 +431,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
     __syncwarp();
   } else if (warp < 12) {
-    regs_inc<136>();
+    regs_inc<128>();
     // --------------------------------------------------------- compute
     // Thread (warpgroup c, lane row r) owns key row r and query columns
     // [64c, 64c + 64) of S^T, P^T, dP^T and dS^T.
@@ -513,6 +521,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     // warpgroup c writes columns [c d/2, (c+1) d/2) of this key row
     bool have = ok && n_it > 0;
     if (have) {
+      // the last dq_full commit covers every MMA, the last dV included
       have = mbar_wait(smem_addr(&bars->dq_full), (n_it - 1) & 1, lim);
       if (!have) record_error(p.err, kErrTimeout);
       tc_fence_after();
@@ -555,7 +564,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       }
     }
   } else {
-    regs_inc<160>();
+    regs_inc<144>();
     // --------------------------------------------------------- dQ (query row r)
     const int r = tid - 384;
     const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;

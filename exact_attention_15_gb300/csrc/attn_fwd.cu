@@ -207,11 +207,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int n_kv = max(t.n[0], t.n[1]);
   const long long lim = p.wait_limit;
 
-  // Register split: 128 x 56 (warps 0-3) + 256 x 224 (softmax) = 384 x 168.
+  // Register split: 128 x 88 (warps 0-3) + 256 x 208 (softmax) = 384 x 168.
   // Each budget change sits inside the branch of the warps it applies to, so the
   // compiler sees which code runs under which budget.
   if (warp < 4) {
-    regs_dec<56>();
+    regs_dec<88>();
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0 && n_kv > 0) {
@@ -248,31 +248,43 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
+    // One thread issues every MMA. Its issue order alternates the two query
+    // tiles (PV_0, S_0, PV_1, S_1, ...), which keeps the two softmax warpgroups
+    // half an iteration apart, so each one's softmax overlaps the other tile's
+    // MMAs. A tcgen05.mma holds the issuing thread for about its own execution
+    // time, so this thread does as little else as possible between MMAs.
     if (lane == 0 && n_kv > 0) {
       constexpr uint32_t kIdS = make_idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t kIdPV = make_idesc_bf16(128, D, 0, 1);
       const uint32_t q_base = smem_addr(smem + Cfg::kQOff);
       const uint32_t kv_base = smem_addr(smem + Cfg::kKVOff);
       bool ok = mbar_wait(smem_addr(&bars->q_full), 0, lim);
+      // Descriptors are built once; each MMA only adds a compile-time byte
+      // offset (>> 4) to the start-address field.
+      const uint64_t q_desc = make_sdesc_sw128(q_base, 16, 1024);     // K-major
+      const uint64_t k_desc = make_sdesc_sw128(kv_base, 16, 1024);    // K-major
+      const uint64_t v_desc = make_sdesc_sw128(kv_base, 16384, 1024); // MN-major
       auto issue_s = [&](int i, int stage) {
-        const uint32_t qa = q_base + i * Cfg::kTileBytes;
-        const uint32_t kb = kv_base + stage * Cfg::kTileBytes;
+        const uint64_t qa = q_desc + ((i * Cfg::kTileBytes) >> 4);
+        const uint64_t kb = k_desc + ((stage * Cfg::kTileBytes) >> 4);
+        const uint32_t d_tmem = tmem + Cfg::kColS0 + i * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + Cfg::kColS0 + i * 128, make_sdesc_sw128(qa + off, 16, 1024),
-                 make_sdesc_sw128(kb + off, 16, 1024), kIdS, kk > 0);
+          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_ss(d_tmem, qa + off, kb + off, kIdS, kk > 0);
         }
         mma_commit(smem_addr(&bars->s_full[i]));
       };
       auto issue_pv = [&](int i, int stage, int j) {
-        const uint32_t vb = kv_base + stage * Cfg::kTileBytes;
+        const uint64_t vb = v_desc + ((stage * Cfg::kTileBytes) >> 4);
+        const uint32_t d_tmem = tmem + Cfg::kColO0 + i * D;
+        const uint32_t a_tmem = tmem + Cfg::kColS0 + i * 128;
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          mma_ts(tmem + Cfg::kColO0 + i * D, tmem + Cfg::kColS0 + i * 128 + kk * 8,
-                 make_sdesc_sw128(vb + kk * 2048, 16384, 1024), kIdPV, (j > 0 || kk > 0));
-        }
-        mma_commit(smem_addr(&bars->pv_done[i]));
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+          mma_ts(d_tmem, a_tmem + kk * 8, vb + kk * (2048 >> 4), kIdPV, (j > 0 || kk > 0));
+        // only the last PV of a tile is signalled (to the epilogue); earlier ones
+        // are covered by the commit of the S MMA issued after them
+        if (j + 1 == t.n[i]) mma_commit(smem_addr(&bars->pv_done[i]));
       };
       // K_j is load number 2j, V_j load number 2j+1.
       auto stage_of = [&](int it) { return it % Cfg::kStages; };
@@ -308,7 +320,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
     __syncwarp();
   } else {
-    regs_inc<224>();
+    regs_inc<208>();
     // ---------------------------------------------------------- softmax + epilogue
     const int i = (warp - 4) >> 2;          // query tile of this warpgroup
     const int r = tid - 128 * (1 + i);      // row within the tile == TMEM lane
@@ -346,9 +358,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         softmax_row_tile<D, 0, false>(s, c, m_used, l, kv0, qrow, t, need_mask, p.causal, pk,
                                       rescale_warp, factor);
       if (rescale_warp && j > 0 && __any_sync(0xffffffffu, factor != 1.0f)) {
-        // correction: O_{j-1} must be complete before it is scaled
-        if (!mbar_wait(smem_addr(&bars->pv_done[i]), (j - 1) & 1, lim)) { ok = false; break; }
-        tc_fence_after();
+        // correction: O_{j-1} is complete here, because the commit that
+        // signalled S_j came from the thread that issued PV_{j-1} before S_j
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t ov[32];
@@ -370,7 +381,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (my_valid) {
       bool have_o = ok && my_n > 0;
       if (have_o) {
-        have_o = mbar_wait(smem_addr(&bars->pv_done[i]), (my_n - 1) & 1, lim);
+        have_o = mbar_wait(smem_addr(&bars->pv_done[i]), 0, lim);
         if (!have_o) record_error(p.err, kErrTimeout);
         tc_fence_after();
       }
