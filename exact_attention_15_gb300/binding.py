@@ -46,7 +46,8 @@ _SIGS = {
 }
 
 KERNEL_NAMES = {1: "attn_fwd_kernel", 2: "attn_bwd_pre_kernel", 3: "attn_bwd_main_kernel",
-                4: "attn_bwd_post_kernel", 5: "exp2_probe_kernel", 6: "stall_probe_kernel"}
+                4: "attn_bwd_post_kernel", 5: "exp2_probe_kernel", 6: "stall_probe_kernel",
+                7: "fwd_plan_kernel"}
 FAULT_NONE = 0
 FAULT_SKIP_DQ_RELEASE = 1
 

@@ -30,10 +30,15 @@ struct FwdParams {
   const int* cu_seqlens;  // nullptr for fixed length
   int B, H_q, H_kv, N_q, N_k, group;
   int causal;
-  int n_mblocks;        // CTA tiles (2 x 128 query rows) per (batch, head) or upper bound (packed)
+  int n_mblocks;        // work tiles (2 x 128 query rows) per (batch, head); fixed length only
   float scale_log2;     // scale * log2(e)
   int* err;             // device error word
   long long wait_limit; // cycles
+  // Work list of the forward (longest-processing-time-first order).
+  const int* seq_order;   // packed: virtual -> actual sequence, longest first
+  const int* tile_start;  // packed: first work tile of each virtual sequence, [B + 1]
+  int total_tiles;        // fixed length: B * n_mblocks * H_q
+  int sec_heads;          // query heads per L2 section (a multiple of H_q / H_kv)
 };
 
 struct BwdParams {
@@ -57,7 +62,7 @@ struct BwdParams {
 // Kernel tracing (host side, implemented next to the C ABI). prof_begin
 // returns a slot (or -1 when tracing is off); prof_end closes it.
 enum KernelId : int { kKFwd = 1, kKBwdPre = 2, kKBwdMain = 3, kKBwdPost = 4, kKExp2 = 5,
-                      kKStall = 6 };
+                      kKStall = 6, kKFwdPlan = 7 };
 int prof_begin(int kernel, cudaStream_t stream);
 void prof_end(int slot, cudaStream_t stream);
 

@@ -1,14 +1,21 @@
 // Forward pass of exact softmax attention for sm_103a.
 //
-// One CTA owns two 128-row query tiles of one (batch, query head) and streams
-// every key/value tile they see through shared memory
+// A work tile is two 128-row query tiles of one (batch, query head); the CTA
+// that owns it streams every key/value tile they see through shared memory
 // (FlashAttention-4 summary, section 3.1.2: two output tiles per CTA, one
 // softmax warpgroup per tile, one thread per row; the FlashAttention-2 loop order
-// with the query tile outside and keys/values inside).
+// with the query tile outside and keys/values inside). Work tiles are numbered
+// in longest-processing-time-first order (section 3.3) and CTA c takes tiles
+// c, c + gridDim.x, c + 2 gridDim.x, ... The host picks the grid: one CTA per
+// work tile when tile lengths differ (causal masks, packed sequences), so the
+// hardware block scheduler hands the tiles out greedily in LPT order; one CTA
+// per SM when they are all equal, so consecutive tiles of a CTA overlap (the
+// next tile's Q and K/V loads and first S MMAs run under the current tile's
+// last P V MMAs and epilogue).
 //
 // Warp roles (384 threads):
-//   warp 0      TMA producer: both Q tiles once, then K_j / V_j into a ring of
-//               single-tile stages (order K0 V0 K1 V1 ...).
+//   warp 0      TMA producer: both Q tiles of a work tile, then K_j / V_j into a
+//               ring of single-tile stages (order K0 V0 K1 V1 ...).
 //   warp 1      TMEM owner and MMA issuer (one thread): S_t = Q_t K_j^T (SS) and
 //               O_t += P_t V_j (TS, P read from TMEM), ping-ponging the tiles so
 //               the tensor core works on one tile while the other is in softmax.
@@ -16,6 +23,8 @@
 //               from TMEM, mask, row max, conditional rescale (tau = 8 in powers
 //               of two, decided per warp), exp2, row sum, P (bf16) back into the S
 //               columns of TMEM, and finally the epilogue O / l and LSE.
+// Every role derives the work tile from (blockIdx.x, k) itself; nothing about
+// the work list passes between roles.
 //
 // TMEM (512 columns): O_0 [0, d), O_1 [d, 2d), S_0/P_0 [2d, 2d+128),
 // S_1/P_1 [2d+128, 2d+256).
@@ -34,25 +43,15 @@ struct FwdCfg {
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = 2 * kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
-  static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+  static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // barriers + alignment slack
   static constexpr uint32_t kColO0 = 0, kColO1 = D;
   static constexpr uint32_t kColS0 = 2 * D, kColS1 = 2 * D + 128;
   static constexpr uint32_t kTmemCols = 512;
 };
 
-struct FwdBars {
-  uint64_t q_full;
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t pv_done[2];
-  uint64_t kv_full[8];
-  uint64_t kv_empty[8];
-  uint32_t tmem_base;
-};
-
-// Work decode shared by every role of the CTA.
+// Work decode: one work tile = two 128-row query tiles of one (batch, query head).
 struct FwdTile {
-  int b, h, h_kv;
+  int b, h, h_kv;  // b < 0 marks the end of the work list
   int q0;          // first query row of tile 0, relative to the sequence
   int row_base;    // global packed-row offset of the sequence (0 for fixed length)
   int batch_coord; // TMA batch coordinate (b for fixed length, 0 for packed)
@@ -61,36 +60,71 @@ struct FwdTile {
   int valid[2];
 };
 
-__device__ __forceinline__ bool decode_fwd_tile(const FwdParams& p, FwdTile& t) {
-  t.h = blockIdx.y;
-  t.h_kv = t.h / p.group;
-  int m;
+// Where a work tile lies: its sequence (batch entry) and its index within that
+// sequence's tiles.
+struct FwdWork {
+  int local;     // tile index within the sequence; < 0 marks the end of the list
+  int b;         // batch entry or packed sequence
+  int row_base;  // first packed row of the sequence (0 for fixed length)
+  int L;         // sequence length (fixed length: N_q)
+};
+
+struct FwdBars {
+  uint64_t q_full, q_empty;
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  uint32_t tmem_base;
+};
+// Longest-processing-time-first order of the work list (FlashAttention-4
+// summary, section 3.3). The batch (for packed inputs: the sequence, taken
+// longest first through seq_order) is outermost; inside it the query heads are
+// cut into sections whose K/V fit in L2; inside a section the m-blocks run
+// longest first (reversed for causal masks) and the heads of the section are
+// innermost, so all query heads of a KV head are visited before the next
+// m-block. locate_fwd_work finds the sequence of work tile v; expand_fwd_work
+// finds the head and m-block inside it.
+__device__ __forceinline__ FwdWork locate_fwd_work(const FwdParams& p, int v) {
+  FwdWork w;
   if (p.cu_seqlens == nullptr) {
-    t.b = blockIdx.z;
-    m = p.causal ? (p.n_mblocks - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
-    t.row_base = 0;
-    t.batch_coord = t.b;
-    t.Lq = p.N_q;
-    t.Lk = p.N_k;
+    const int per_b = p.n_mblocks * p.H_q;
+    w.b = v / per_b;
+    w.local = v - w.b * per_b;
+    w.row_base = 0;
+    w.L = p.N_q;
   } else {
-    int idx = blockIdx.x;
-    int s = 0;
-    int L = 0;
-    for (; s < p.B; ++s) {
-      L = p.cu_seqlens[s + 1] - p.cu_seqlens[s];
-      const int nt = (L + 2 * kTileM - 1) / (2 * kTileM);
-      if (idx < nt) break;
-      idx -= nt;
+    // largest virtual sequence whose first tile is <= v (sequences without
+    // tiles share their start with the next one and are never selected)
+    int lo = 0, hi = p.B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (p.tile_start[mid] <= v) lo = mid; else hi = mid;
     }
-    if (s >= p.B) return false;
-    const int nt = (L + 2 * kTileM - 1) / (2 * kTileM);
-    m = p.causal ? (nt - 1 - idx) : idx;
-    t.b = s;
-    t.row_base = p.cu_seqlens[s];
-    t.batch_coord = 0;
-    t.Lq = L;
-    t.Lk = L;
+    w.b = p.seq_order[lo];
+    w.local = v - p.tile_start[lo];
+    w.row_base = p.cu_seqlens[w.b];
+    w.L = p.cu_seqlens[w.b + 1] - w.row_base;
   }
+  return w;
+}
+
+__device__ __forceinline__ void expand_fwd_work(const FwdParams& p, const FwdWork& w, FwdTile& t) {
+  t.b = w.b;
+  t.row_base = w.row_base;
+  t.batch_coord = p.cu_seqlens ? 0 : w.b;
+  t.Lq = w.L;
+  t.Lk = p.cu_seqlens ? w.L : p.N_k;
+  const int nm = (w.L + 2 * kTileM - 1) / (2 * kTileM);
+  const int sec = w.local / (nm * p.sec_heads);
+  const int r = w.local - sec * nm * p.sec_heads;
+  const int h0 = sec * p.sec_heads;
+  const int hs = min(p.sec_heads, p.H_q - h0);
+  const int mi = r / hs;
+  t.h = h0 + (r - mi * hs);
+  t.h_kv = t.h / p.group;
+  const int m = p.causal ? (nm - 1 - mi) : mi;
   t.q0 = m * 2 * kTileM;
   for (int i = 0; i < 2; ++i) {
     const int r0 = t.q0 + i * kTileM;
@@ -99,13 +133,21 @@ __device__ __forceinline__ bool decode_fwd_tile(const FwdParams& p, FwdTile& t) 
     if (p.causal) kv_end = min(kv_end, r0 + kTileM);
     t.n[i] = t.valid[i] ? (kv_end + kTileN - 1) / kTileN : 0;
   }
+}
+
+// The k-th work tile of this CTA; false past the end of the list.
+__device__ __forceinline__ bool next_tile(const FwdParams& p, int k, FwdTile& t) {
+  const int v = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+  const int total = p.cu_seqlens ? p.tile_start[p.B] : p.total_tiles;
+  if (v >= total) return false;
+  expand_fwd_work(p, locate_fwd_work(p, v), t);
   return true;
 }
 
 // ------------------------------------------------------------------ softmax
 template <int D, int EMU, bool POS_SCALE>
 __device__ __forceinline__ void softmax_row_tile(float (&s)[128], float c, float& m_used,
-                                                 float& l, int kv0, int qrow, const FwdTile& t,
+                                                 float& l, int kv0, int qrow, int Lk,
                                                  bool need_mask, int causal,
                                                  uint32_t (&pk)[64], bool& rescale_warp,
                                                  float& factor) {
@@ -117,7 +159,7 @@ __device__ __forceinline__ void softmax_row_tile(float (&s)[128], float c, float
 #pragma unroll
     for (int i = 0; i < 128; ++i) {
       const int key = kv0 + i;
-      const bool vis = key < t.Lk && (!causal || key <= qrow);
+      const bool vis = key < Lk && (!causal || key <= qrow);
       s[i] = vis ? s[i] : -INFINITY;
     }
   }
@@ -176,15 +218,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   FwdBars* bars = reinterpret_cast<FwdBars*>(smem + Cfg::kBarOff);
 
-  FwdTile t;
-  if (!decode_fwd_tile(p, t)) return;  // packed inputs: grid is an upper bound
-
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
   if (tid == 0) {
     mbar_init(smem_addr(&bars->q_full), 1);
+    mbar_init(smem_addr(&bars->q_empty), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&bars->s_full[i]), 1);
       mbar_init(smem_addr(&bars->p_full[i]), 128);
@@ -204,9 +244,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const int n_kv = max(t.n[0], t.n[1]);
   const long long lim = p.wait_limit;
 
+  // Every role walks the same sequence of work tiles. Barrier phases carry on
+  // across tiles, so each role counts its own waits.
+  //
   // Register split: 128 x 88 (warps 0-3) + 256 x 208 (softmax) = 384 x 168.
   // Each budget change sits inside the branch of the warps it applies to, so the
   // compiler sees which code runs under which budget.
@@ -214,36 +256,53 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     regs_dec<88>();
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
-    if (lane == 0 && n_kv > 0) {
+    if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const uint32_t qbar = smem_addr(&bars->q_full);
-      const int nq = (t.n[0] > 0) + (t.n[1] > 0);
-      mbar_arrive_expect_tx(qbar, nq * Cfg::kTileBytes);
+      uint32_t ld = 0;  // K/V loads issued so far (K_j, V_j of each tile in turn)
+      int qk = 0;       // tiles whose Q was loaded (tiles that see no key load nothing)
+      FwdTile t;
+      bool ok = true;
+      for (int k = 0; ok && next_tile(p, k, t); ++k) {
+        const int n_kv = max(t.n[0], t.n[1]);
+        if (n_kv > 0) {
+          // Q of this tile goes into the buffer once the previous tile's last
+          // S MMA has read it
+          if (qk > 0 && !mbar_wait(smem_addr(&bars->q_empty), (qk - 1) & 1, lim)) {
+            record_error(p.err, kErrTimeout);
+            break;
+          }
+          ++qk;
+          const uint32_t qbar = smem_addr(&bars->q_full);
+          const int nq = (t.n[0] > 0) + (t.n[1] > 0);
+          mbar_arrive_expect_tx(qbar, nq * Cfg::kTileBytes);
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        if (t.n[i] == 0) continue;
-        const uint32_t dst = smem_addr(smem + Cfg::kQOff + i * Cfg::kTileBytes);
-        for (int hf = 0; hf < Cfg::kHalves; ++hf)
-          tma_load_4d(dst + hf * 16384, &tm_q, qbar, hf * 64, t.h, t.row_base + t.q0 + i * kTileM,
-                      t.batch_coord);
-      }
-      for (int it = 0; it < 2 * n_kv; ++it) {
-        const int j = it >> 1;
-        const int stage = it % Cfg::kStages;
-        const int round = it / Cfg::kStages;
-        if (!mbar_wait(smem_addr(&bars->kv_empty[stage]), (round & 1) ^ 1, lim)) {
-          record_error(p.err, kErrTimeout);
-          break;
+          for (int i = 0; i < 2; ++i) {
+            if (t.n[i] == 0) continue;
+            const uint32_t dst = smem_addr(smem + Cfg::kQOff + i * Cfg::kTileBytes);
+            for (int hf = 0; hf < Cfg::kHalves; ++hf)
+              tma_load_4d(dst + hf * 16384, &tm_q, qbar, hf * 64, t.h,
+                          t.row_base + t.q0 + i * kTileM, t.batch_coord);
+          }
+          for (int it = 0; it < 2 * n_kv; ++it, ++ld) {
+            const int j = it >> 1;
+            const uint32_t stage = ld % Cfg::kStages;
+            const uint32_t round = ld / Cfg::kStages;
+            if (!mbar_wait(smem_addr(&bars->kv_empty[stage]), (round & 1) ^ 1, lim)) {
+              record_error(p.err, kErrTimeout);
+              ok = false;
+              break;
+            }
+            const uint32_t fbar = smem_addr(&bars->kv_full[stage]);
+            mbar_arrive_expect_tx(fbar, Cfg::kTileBytes);
+            const uint32_t dst = smem_addr(smem + Cfg::kKVOff + stage * Cfg::kTileBytes);
+            const CUtensorMap* map = (it & 1) ? &tm_v : &tm_k;
+            for (int hf = 0; hf < Cfg::kHalves; ++hf)
+              tma_load_4d(dst + hf * 16384, map, fbar, hf * 64, t.h_kv, t.row_base + j * kTileN,
+                          t.batch_coord);
+          }
         }
-        const uint32_t fbar = smem_addr(&bars->kv_full[stage]);
-        mbar_arrive_expect_tx(fbar, Cfg::kTileBytes);
-        const uint32_t dst = smem_addr(smem + Cfg::kKVOff + stage * Cfg::kTileBytes);
-        const CUtensorMap* map = (it & 1) ? &tm_v : &tm_k;
-        for (int hf = 0; hf < Cfg::kHalves; ++hf)
-          tma_load_4d(dst + hf * 16384, map, fbar, hf * 64, t.h_kv, t.row_base + j * kTileN,
-                      t.batch_coord);
       }
     }
   } else if (warp == 1) {
@@ -253,18 +312,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // half an iteration apart, so each one's softmax overlaps the other tile's
     // MMAs. A tcgen05.mma holds the issuing thread for about its own execution
     // time, so this thread does as little else as possible between MMAs.
-    if (lane == 0 && n_kv > 0) {
+    if (lane == 0) {
       constexpr uint32_t kIdS = make_idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t kIdPV = make_idesc_bf16(128, D, 0, 1);
       const uint32_t q_base = smem_addr(smem + Cfg::kQOff);
       const uint32_t kv_base = smem_addr(smem + Cfg::kKVOff);
-      bool ok = mbar_wait(smem_addr(&bars->q_full), 0, lim);
       // Descriptors are built once; each MMA only adds a compile-time byte
       // offset (>> 4) to the start-address field.
       const uint64_t q_desc = make_sdesc_sw128(q_base, 16, 1024);     // K-major
       const uint64_t k_desc = make_sdesc_sw128(kv_base, 16, 1024);    // K-major
       const uint64_t v_desc = make_sdesc_sw128(kv_base, 16384, 1024); // MN-major
-      auto issue_s = [&](int i, int stage) {
+      auto issue_s = [&](int i, uint32_t stage) {
         const uint64_t qa = q_desc + ((i * Cfg::kTileBytes) >> 4);
         const uint64_t kb = k_desc + ((stage * Cfg::kTileBytes) >> 4);
         const uint32_t d_tmem = tmem + Cfg::kColS0 + i * 128;
@@ -275,45 +333,60 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         mma_commit(smem_addr(&bars->s_full[i]));
       };
-      auto issue_pv = [&](int i, int stage, int j) {
+      auto issue_pv = [&](int i, uint32_t stage, bool acc) {
         const uint64_t vb = v_desc + ((stage * Cfg::kTileBytes) >> 4);
         const uint32_t d_tmem = tmem + Cfg::kColO0 + i * D;
         const uint32_t a_tmem = tmem + Cfg::kColS0 + i * 128;
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)
-          mma_ts(d_tmem, a_tmem + kk * 8, vb + kk * (2048 >> 4), kIdPV, (j > 0 || kk > 0));
-        // only the last PV of a tile is signalled (to the epilogue); earlier ones
-        // are covered by the commit of the S MMA issued after them
-        if (j + 1 == t.n[i]) mma_commit(smem_addr(&bars->pv_done[i]));
+          mma_ts(d_tmem, a_tmem + kk * 8, vb + kk * (2048 >> 4), kIdPV, (acc || kk > 0));
       };
-      // K_j is load number 2j, V_j load number 2j+1.
-      auto stage_of = [&](int it) { return it % Cfg::kStages; };
-      auto phase_of = [&](int it) { return (it / Cfg::kStages) & 1; };
-      if (ok) ok = mbar_wait(smem_addr(&bars->kv_full[stage_of(0)]), phase_of(0), lim);
-      if (ok) {
+      uint32_t ld = 0;     // K/V loads consumed so far, in the producer's order
+      int pw[2] = {0, 0};  // p_full waits so far, per query tile
+      int qk = 0;          // tiles with a Q load
+      bool ok = true;
+      FwdTile t;
+      for (int k = 0; ok && next_tile(p, k, t); ++k) {
+        const int n_kv = max(t.n[0], t.n[1]);
+        if (n_kv == 0) continue;  // no keys: the epilogue writes O = 0, LSE = -inf
+        // K_j is load ld + 2j, V_j load ld + 2j + 1
+        auto stage_of = [&](int it) { return (ld + it) % Cfg::kStages; };
+        auto phase_of = [&](int it) { return ((ld + it) / Cfg::kStages) & 1; };
+        ok = mbar_wait(smem_addr(&bars->q_full), qk & 1, lim);
+        ++qk;
+        if (ok) ok = mbar_wait(smem_addr(&bars->kv_full[stage_of(0)]), phase_of(0), lim);
+        if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int i = 0; i < 2; ++i)
           if (t.n[i] > 0) issue_s(i, stage_of(0));
         mma_commit(smem_addr(&bars->kv_empty[stage_of(0)]));
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int itv = 2 * j + 1, itk = 2 * j + 2;
-        const bool next_k = (j + 1) < n_kv;
-        ok = mbar_wait(smem_addr(&bars->kv_full[stage_of(itv)]), phase_of(itv), lim);
-        if (ok && next_k) ok = mbar_wait(smem_addr(&bars->kv_full[stage_of(itk)]), phase_of(itk), lim);
-        if (!ok) break;
+        // Q is free again once the tile's last S MMA is done
+        if (n_kv == 1) mma_commit(smem_addr(&bars->q_empty));
+        for (int j = 0; j < n_kv; ++j) {
+          const int itv = 2 * j + 1, itk = 2 * j + 2;
+          const bool next_k = (j + 1) < n_kv;
+          ok = mbar_wait(smem_addr(&bars->kv_full[stage_of(itv)]), phase_of(itv), lim);
+          if (ok && next_k) ok = mbar_wait(smem_addr(&bars->kv_full[stage_of(itk)]), phase_of(itk), lim);
+          if (!ok) break;
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          if (j >= t.n[i]) continue;
-          if (!mbar_wait(smem_addr(&bars->p_full[i]), j & 1, lim)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(i, stage_of(itv), j);
-          if (j + 1 < t.n[i]) issue_s(i, stage_of(itk));
+          for (int i = 0; i < 2; ++i) {
+            if (j >= t.n[i]) continue;
+            if (!mbar_wait(smem_addr(&bars->p_full[i]), pw[i] & 1, lim)) { ok = false; break; }
+            ++pw[i];
+            tc_fence_after();
+            issue_pv(i, stage_of(itv), j > 0);
+            // only the last PV of a tile is signalled (to the epilogue); earlier
+            // ones are covered by the commit of the S MMA issued after them
+            if (j + 1 == t.n[i]) mma_commit(smem_addr(&bars->pv_done[i]));
+            else issue_s(i, stage_of(itk));
+          }
+          if (!ok) break;
+          mma_commit(smem_addr(&bars->kv_empty[stage_of(itv)]));
+          if (next_k) mma_commit(smem_addr(&bars->kv_empty[stage_of(itk)]));
+          if (j + 2 == n_kv) mma_commit(smem_addr(&bars->q_empty));
         }
-        if (!ok) break;
-        mma_commit(smem_addr(&bars->kv_empty[stage_of(itv)]));
-        if (next_k) mma_commit(smem_addr(&bars->kv_empty[stage_of(itk)]));
+        ld += 2 * n_kv;
       }
       if (!ok) record_error(p.err, kErrTimeout);
     }
@@ -327,99 +400,111 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t lane_base = static_cast<uint32_t>((r & ~31)) << 16;
     const uint32_t col_s = i ? Cfg::kColS1 : Cfg::kColS0;
     const uint32_t col_o = i ? Cfg::kColO1 : Cfg::kColO0;
-    const int qrow = t.q0 + i * kTileM + r;  // sequence-relative query row
-    const int my_n = i ? t.n[1] : t.n[0];
-    const int my_valid = i ? t.valid[1] : t.valid[0];
     const float c = p.scale_log2;
-    float m_used = -INFINITY;
-    float l = 0.0f;
+    int sw = 0;   // s_full waits so far
+    int pvw = 0;  // pv_done waits so far
     bool ok = true;
-    for (int j = 0; j < my_n; ++j) {
-      if (!mbar_wait(smem_addr(&bars->s_full[i]), j & 1, lim)) { ok = false; break; }
-      tc_fence_after();
-      float s[128];
-      {
-        uint32_t* sr = reinterpret_cast<uint32_t*>(s);
+    for (int k = 0; ok; ++k) {
+      FwdTile t;
+      if (!next_tile(p, k, t)) break;
+      const int my_n = i ? t.n[1] : t.n[0];
+      const int Lk = t.Lk;
+      const int q0i = t.q0 + i * kTileM;   // first row of this warpgroup's query tile
+      const int qrow = q0i + r;            // sequence-relative query row
+      float m_used = -INFINITY;
+      float l = 0.0f;
+      for (int j = 0; j < my_n; ++j) {
+        if (!mbar_wait(smem_addr(&bars->s_full[i]), sw & 1, lim)) { ok = false; break; }
+        ++sw;
+        tc_fence_after();
+        float s[128];
+        {
+          uint32_t* sr = reinterpret_cast<uint32_t*>(s);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-          tmem_ld32(tmem + lane_base + col_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + cc * 32));
+          for (int cc = 0; cc < 4; ++cc)
+            tmem_ld32(tmem + lane_base + col_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + cc * 32));
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + cc * 32));
+          for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + cc * 32));
+        }
+        const int kv0 = j * kTileN;
+        const bool need_mask = (kv0 + kTileN > Lk) || (p.causal && kv0 + kTileN - 1 > q0i);
+        uint32_t pk[64];
+        bool rescale_warp;
+        float factor;
+        if (c > 0.0f)
+          softmax_row_tile<D, EMU, true>(s, c, m_used, l, kv0, qrow, Lk, need_mask, p.causal, pk,
+                                         rescale_warp, factor);
+        else
+          softmax_row_tile<D, 0, false>(s, c, m_used, l, kv0, qrow, Lk, need_mask, p.causal, pk,
+                                        rescale_warp, factor);
+        if (rescale_warp && j > 0 && __any_sync(0xffffffffu, factor != 1.0f)) {
+          // correction: O_{j-1} is complete here, because the commit that
+          // signalled S_j came from the thread that issued PV_{j-1} before S_j
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t ov[32];
+            tmem_ld32(tmem + lane_base + col_o + cc * 32, ov);
+            tmem_ld_wait(ov);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
+            tmem_st32(tmem + lane_base + col_o + cc * 32, ov);
+          }
+        }
+        tmem_st32(tmem + lane_base + col_s, *reinterpret_cast<uint32_t(*)[32]>(pk));
+        tmem_st32(tmem + lane_base + col_s + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_addr(&bars->p_full[i]));
       }
-      const int kv0 = j * kTileN;
-      const bool need_mask = (kv0 + kTileN > t.Lk) || (p.causal && kv0 + kTileN - 1 > t.q0 + i * kTileM);
-      uint32_t pk[64];
-      bool rescale_warp;
-      float factor;
-      if (c > 0.0f)
-        softmax_row_tile<D, EMU, true>(s, c, m_used, l, kv0, qrow, t, need_mask, p.causal, pk,
-                                       rescale_warp, factor);
-      else
-        softmax_row_tile<D, 0, false>(s, c, m_used, l, kv0, qrow, t, need_mask, p.causal, pk,
-                                      rescale_warp, factor);
-      if (rescale_warp && j > 0 && __any_sync(0xffffffffu, factor != 1.0f)) {
-        // correction: O_{j-1} is complete here, because the commit that
-        // signalled S_j came from the thread that issued PV_{j-1} before S_j
+      if (!ok) break;
+      // -------------------------------------------------------- epilogue
+      // The O columns are reused by the next tile's first PV MMA, which waits
+      // for this warpgroup's next p_full arrival, i.e. after these loads.
+      if (i ? t.valid[1] : t.valid[0]) {
+        bool have_o = my_n > 0;
+        if (have_o) {
+          have_o = mbar_wait(smem_addr(&bars->pv_done[i]), pvw & 1, lim);
+          ++pvw;
+          if (!have_o) { ok = false; break; }
+          tc_fence_after();
+        }
+        const bool row_ok = qrow < t.Lq;
+        const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
+        const size_t grow = static_cast<size_t>(t.row_base) + qrow;  // packed row
+        const size_t o_off =
+            p.cu_seqlens ? (grow * p.H_q + t.h) * D
+                         : ((static_cast<size_t>(t.b) * p.N_q + qrow) * p.H_q + t.h) * D;
+        uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + o_off);
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t ov[32];
-          tmem_ld32(tmem + lane_base + col_o + cc * 32, ov);
-          tmem_ld_wait(ov);
+          if (have_o) {
+            tmem_ld32(tmem + lane_base + col_o + cc * 32, ov);
+            tmem_ld_wait(ov);
+          } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * factor);
-          tmem_st32(tmem + lane_base + col_o + cc * 32, ov);
+            for (int e = 0; e < 32; ++e) ov[e] = 0u;
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
+          if (row_ok) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              orow[cc * 4 + e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          }
+        }
+        if (row_ok) {
+          const float lse = (l > 0.0f) ? (m_used * kLn2 + __logf(l)) : -INFINITY;
+          const size_t l_off = p.cu_seqlens
+                                   ? static_cast<size_t>(t.h) * p.N_q + grow
+                                   : (static_cast<size_t>(t.b) * p.H_q + t.h) * p.N_q + qrow;
+          p.lse[l_off] = lse;
         }
       }
-      tmem_st32(tmem + lane_base + col_s, *reinterpret_cast<uint32_t(*)[32]>(pk));
-      tmem_st32(tmem + lane_base + col_s + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(smem_addr(&bars->p_full[i]));
     }
     if (!ok) record_error(p.err, kErrTimeout);
-    // ---------------------------------------------------------- epilogue
-    if (my_valid) {
-      bool have_o = ok && my_n > 0;
-      if (have_o) {
-        have_o = mbar_wait(smem_addr(&bars->pv_done[i]), 0, lim);
-        if (!have_o) record_error(p.err, kErrTimeout);
-        tc_fence_after();
-      }
-      const bool row_ok = qrow < t.Lq;
-      const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
-      const size_t grow = static_cast<size_t>(t.row_base) + qrow;  // packed row
-      const size_t o_off =
-          p.cu_seqlens ? (grow * p.H_q + t.h) * D
-                       : ((static_cast<size_t>(t.b) * p.N_q + qrow) * p.H_q + t.h) * D;
-      uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + o_off);
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t ov[32];
-        if (have_o) {
-          tmem_ld32(tmem + lane_base + col_o + cc * 32, ov);
-          tmem_ld_wait(ov);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = 0u;
-        }
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          w[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
-        if (row_ok) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            orow[cc * 4 + e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-        }
-      }
-      if (row_ok) {
-        const float lse = (l > 0.0f) ? (m_used * kLn2 + __logf(l)) : -INFINITY;
-        const size_t l_off = p.cu_seqlens
-                                 ? static_cast<size_t>(t.h) * p.N_q + grow
-                                 : (static_cast<size_t>(t.b) * p.H_q + t.h) * p.N_q + qrow;
-        p.lse[l_off] = lse;
-      }
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -427,6 +512,74 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::kTmemCols);
   }
+}
+
+// Orders packed sequences longest first (their longest work tile is the
+// longest) and writes the forward's work-list metadata: seq_order maps a
+// virtual sequence index to the actual one and tile_start[v] is the first work
+// tile of virtual sequence v (FlashAttention-4 summary, section 3.3, the
+// varlen scheduling paragraph). One CTA. Ties keep their input order; with
+// sort == 0 the input order is kept.
+__global__ void __launch_bounds__(1024)
+fwd_plan_kernel(const int* __restrict__ cu_seqlens, int B, int H_q, int sort, int* seq_order,
+                int* tile_start) {
+  extern __shared__ int plan_smem[];
+  int* len = plan_smem;        // [B] when sorting
+  int* ord = plan_smem + B;    // [B] when sorting
+  __shared__ int warp_sum[32];
+  const int tid = threadIdx.x;
+  if (sort) {
+    for (int s = tid; s < B; s += blockDim.x) len[s] = cu_seqlens[s + 1] - cu_seqlens[s];
+    __syncthreads();
+    for (int s = tid; s < B; s += blockDim.x) {
+      const int L = len[s];
+      int rank = 0;
+      for (int u = 0; u < B; ++u) {
+        const int Lu = len[u];
+        rank += (Lu > L) || (Lu == L && u < s);
+      }
+      ord[rank] = s;
+    }
+    __syncthreads();
+  }
+  // exclusive prefix of the work tiles per virtual sequence: each thread owns a
+  // contiguous chunk, chunk sums are scanned across the block
+  const int chunk = (B + blockDim.x - 1) / blockDim.x;
+  const int v0 = min(B, tid * chunk), v1 = min(B, v0 + chunk);
+  auto tiles_of = [&](int vs) {
+    const int s = sort ? ord[vs] : vs;
+    const int L = sort ? len[s] : (cu_seqlens[s + 1] - cu_seqlens[s]);
+    return (L + 2 * kTileM - 1) / (2 * kTileM) * H_q;
+  };
+  int local = 0;
+  for (int vs = v0; vs < v1; ++vs) local += tiles_of(vs);
+  const int lane = tid & 31, w = tid >> 5;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sum[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    const int nw = blockDim.x >> 5;
+    int x = lane < nw ? warp_sum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane < nw) warp_sum[lane] = x;  // inclusive over warps
+  }
+  __syncthreads();
+  int run = incl - local + (w > 0 ? warp_sum[w - 1] : 0);
+  for (int vs = v0; vs < v1; ++vs) {
+    seq_order[vs] = sort ? ord[vs] : vs;
+    tile_start[vs] = run;
+    run += tiles_of(vs);
+  }
+  if (tid == blockDim.x - 1) tile_start[B] = warp_sum[(blockDim.x >> 5) - 1];
 }
 
 // ------------------------------------------------------------------ host side
@@ -440,6 +593,7 @@ static cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk,
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
+  static_assert(sizeof(FwdBars) <= 512, "barrier block overflows its reservation");
   const int slot = prof_begin(kKFwd, stream);
   kern<<<grid, 384, Cfg::kSmemBytes, stream>>>(tq, tk, tv, p);
   e = cudaGetLastError();
@@ -457,6 +611,24 @@ cudaError_t launch_attn_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             cudaStream_t stream) {
   if (d == 64) return launch_fwd_impl<64, ATTN_FWD_EMU>(tq, tk, tv, p, grid, stream);
   return launch_fwd_impl<128, ATTN_FWD_EMU>(tq, tk, tv, p, grid, stream);
+}
+
+// Largest packed batch the plan kernel sorts (its lengths and order sit in
+// shared memory); larger batches keep their input order.
+constexpr int kPlanMaxSort = 8192;
+
+cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int H_q, int* seq_order,
+                            int* tile_start, cudaStream_t stream) {
+  const int sort = (B <= kPlanMaxSort) ? 1 : 0;
+  const size_t smem = sort ? static_cast<size_t>(2) * B * sizeof(int) : 0;
+  cudaError_t e = cudaFuncSetAttribute(fwd_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       2 * kPlanMaxSort * static_cast<int>(sizeof(int)));
+  if (e != cudaSuccess) return e;
+  const int slot = prof_begin(kKFwdPlan, stream);
+  fwd_plan_kernel<<<1, 1024, smem, stream>>>(cu_seqlens, B, H_q, sort, seq_order, tile_start);
+  e = cudaGetLastError();
+  prof_end(slot, stream);
+  return e;
 }
 
 // ------------------------------------------------------------------ exp2 test hook

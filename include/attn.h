@@ -82,7 +82,15 @@ typedef enum {
  * finite value is accepted). A query row that sees no key (only possible with
  * empty sequences) gets O = 0 and LSE = -inf.
  * FlashAttention-4 summary, sections 2.1 (definition), 3.1.2 (pipeline),
- * 3.1.4 (online softmax with conditional rescaling).
+ * 3.1.4 (online softmax with conditional rescaling), 3.3 (work tiles are taken
+ * longest first).
+ *
+ * Packed inputs: the call first launches a one-CTA planning kernel that orders
+ * the sequences longest first. It writes into a library-owned device buffer
+ * (cudaMalloc'd on the first packed call on each device and stream, kept until
+ * the process exits; a later call with more sequences than the buffer holds
+ * synchronises that stream once and reallocates it). Make the first packed call
+ * on a stream outside stream capture.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H_q, int H_kv, int N_q, int N_k, int d, int causal,
@@ -199,7 +207,8 @@ long long attn_set_wait_limit(long long cycles);
  * `max_records` records (oldest first) and discards everything it has read;
  * it returns the number of records written, or a negative attn_status.
  * Kernel ids: 1 forward, 2 backward pre (D, zeroing), 3 backward main,
- * 4 backward post (dQ conversion), 5 exp2 test hook, 6 stall test hook.
+ * 4 backward post (dQ conversion), 5 exp2 test hook, 6 stall test hook, 7 forward
+ * planning kernel (packed inputs).
  */
 typedef struct {
   int kernel;  /* kernel id, see above */

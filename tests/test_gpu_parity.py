@@ -91,6 +91,12 @@ SMALL = {
                          boost_frac=0.05, boost=3.0),
     "negative_scale": dict(B=1, H_q=1, H_kv=1, N_q=256, N_k=256, d=64, scale=-0.2, causal=False),
     "zero_scale": dict(B=1, H_q=1, H_kv=1, N_q=130, N_k=130, d=64, scale=0.0, causal=True),
+    # packed lengths out of order, with empty sequences: the forward's work list
+    # visits them longest first
+    "varlen_unsorted_empty": dict(B=0, H_q=4, H_kv=2, N_q=0, N_k=0, d=64, causal=True,
+                                  seqlens=[0, 700, 3, 0, 256, 1000, 0, 257]),
+    # more work tiles (3 x 8 x 8 = 192) than SMs: each persistent CTA takes several
+    "more_tiles_than_sms": dict(B=3, H_q=8, H_kv=4, N_q=2000, N_k=2000, d=64, causal=True),
 }
 
 
@@ -134,6 +140,44 @@ def test_worked_example_on_gpu(d):
         assert abs(float(lse.cpu()[0, 0, 0]) - ref_lse) < 2e-3
 
 
+def test_forward_on_concurrent_streams():
+    """Forward passes issued on two streams at once (each stream has its own work
+    counter) give the same bits as the same passes run one after the other, and
+    repeated launches on one stream reuse the counter correctly."""
+    import torch
+    from exact_attention_15_gb300 import binding
+    probs = [W.custom(seed=s, B=2, H_q=8, H_kv=8, N_q=1500, N_k=1500, d=64, causal=c,
+                      parts=("q", "k", "v"))
+             for s, c in ((11, True), (12, False))]
+    devs = [device_inputs_fwd(x) for x in probs]
+    ref = []
+    for x, dv in zip(probs, devs):
+        o, lse = binding.forward(dv["q"], dv["k"], dv["v"], scale=x.scale, causal=x.causal)
+        torch.cuda.synchronize()
+        ref.append((o.clone(), lse.clone()))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [[], []]
+    torch.cuda.synchronize()
+    for rep in range(4):
+        for i in range(2):
+            with torch.cuda.stream(streams[i]):
+                x, dv = probs[i], devs[i]
+                outs[i].append(binding.forward(dv["q"], dv["k"], dv["v"], scale=x.scale,
+                                               causal=x.causal))
+    torch.cuda.synchronize()
+    assert binding.attn_check(None) == 0
+    for i in range(2):
+        for o, lse in outs[i]:
+            assert torch.equal(o.view(torch.int16), ref[i][0].view(torch.int16))
+            assert torch.equal(lse, ref[i][1])
+    _oracle_fwd_check(probs[0], ref[0][0], ref[0][1], [(0, 0), (1, 7)])
+
+
+def device_inputs_fwd(inp):
+    from gpu_common import to_dev
+    return dict(q=to_dev(inp.q), k=to_dev(inp.k), v=to_dev(inp.v))
+
+
 def test_no_keys_and_empty_batch():
     import torch
     from exact_attention_15_gb300 import binding
@@ -141,11 +185,13 @@ def test_no_keys_and_empty_batch():
     k = torch.empty(1, 0, 2, 64, device="cuda", dtype=torch.bfloat16)
     o, lse = binding.forward(q, k, k)
     torch.cuda.synchronize()
+    assert binding.attn_check(None) == 0
     assert torch.all(o == 0)
     assert torch.all(torch.isinf(lse)) and torch.all(lse < 0)
     q0 = torch.empty(0, 5, 2, 64, device="cuda", dtype=torch.bfloat16)
     binding.forward(q0, q0, q0)
     torch.cuda.synchronize()
+    assert binding.attn_check(None) == 0
 
 
 # ------------------------------------------------------------------ full-size workloads
