@@ -157,7 +157,7 @@ bool fwd_persistent(long long tiles, int n_sm, bool causal, bool varlen, long lo
 // Query heads per L2 section of the forward work list: as many whole KV-head
 // groups as keep their K and V (rows x d bf16 each) within a share of L2, cut
 // evenly over the KV heads.
-int fwd_section_heads(int H_q, int H_kv, long long rows, int d) {
+int l2_section_heads(int H_q, int H_kv, long long rows, int d) {
   constexpr long long kBudget = 48ll << 20;
   const long long per_kv = 2ll * rows * d * 2;
   long long fit = per_kv > 0 ? kBudget / per_kv : H_kv;
@@ -393,7 +393,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.total_tiles = static_cast<int>(tiles);
   p.n_mblocks = (N_q + 255) / 256;
   // the mean sequence length sizes the L2 sections of packed inputs
-  p.sec_heads = fwd_section_heads(H_q, H_kv, seqlens ? (N_k + B - 1) / B : N_k, d);
+  p.sec_heads = l2_section_heads(H_q, H_kv, seqlens ? (N_k + B - 1) / B : N_k, d);
   if (seqlens) {
     PlanBuf pb;
     if ((st = plan_buffer(dev, cs, B, &pb)) != ATTN_OK) return st;
