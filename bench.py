@@ -9,7 +9,8 @@ Prints one JSON line. ``value`` is whole-job attention TFLOP/s (forward
 4*N^2*d per head plus backward 2.5x that), inputs resident in device memory;
 ``e2e`` is the same metric through the public binding with host buffers, the
 host->device copies of q, k, v, dO and the device->host copies of o, lse, dq,
-dk, dv inside the timed region. ``--impl reference`` times the fp64 CPU oracle
+dk, dv of every step inside the timed region (copies overlapped with the
+neighbouring steps' compute; the serial figure is reported beside it). ``--impl reference`` times the fp64 CPU oracle
 on a bounded sample of the same workload.
 """
 
@@ -318,35 +319,93 @@ def main():
     roofline = roof(dominant, flops_of.get(dominant, 0.0)) if dominant in flops_of else None
     roofline_fwd = roof("attn_fwd_kernel", fwd_flops)
 
-    # end to end through the public binding with host buffers
+    # end to end through the public binding with host buffers: every step copies
+    # its inputs (q, k, v, dO) from pinned host memory and its results (o, lse,
+    # dq, dk, dv) back. Timed two ways: serial (copy in, compute, copy out on one
+    # stream) and pipelined (double-buffered device sets, with the copies on their
+    # own streams, so step s+1's inputs and step s-1's results move while step s
+    # computes).
     e2e = None
     if not args.no_e2e:
         hq = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (inp.q, inp.k, inp.v, inp.do)]
-        ho = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
-        hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-        hdq, hdk, hdv = (torch.empty(t.shape, dtype=torch.bfloat16).pin_memory() for t in (q, k, v))
+        hout = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (o, lse, dq, dk, dv)]
+                for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in hq)
-        d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+        d2h = sum(t.numel() * t.element_size() for t in hout[0])
+        sets = [dict(q=q, k=k, v=v, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv)]
+        sets.append({n: torch.empty_like(t) for n, t in sets[0].items()})
 
-        def e2e_step():
-            for hsrc, ddst in zip(hq, (q, k, v, do)):
-                ddst.copy_(hsrc, non_blocking=True)
-            step()
-            for dsrc, hdst in ((o, ho), (lse, hl), (dq, hdq), (dk, hdk), (dv, hdv)):
-                hdst.copy_(dsrc, non_blocking=True)
+        def run_step(st_, sp_):
+            r = binding.attn_fwd(st_["q"].data_ptr(), st_["k"].data_ptr(), st_["v"].data_ptr(),
+                                 st_["o"].data_ptr(), st_["lse"].data_ptr(), B, H, H_kv, N, N, d,
+                                 w.causal, cu_ptr, w.scale, sp_)
+            assert r == 0, r
+            r = binding.attn_bwd(st_["q"].data_ptr(), st_["k"].data_ptr(), st_["v"].data_ptr(),
+                                 st_["o"].data_ptr(), st_["lse"].data_ptr(), st_["do"].data_ptr(),
+                                 st_["dq"].data_ptr(), st_["dk"].data_ptr(), st_["dv"].data_ptr(),
+                                 B, H, H_kv, N, N, d, w.causal, cu_ptr, w.scale, 0, ws.data_ptr(),
+                                 ws_bytes, sp_)
+            assert r == 0, r
+
+        def copy_in(st_):
+            for hsrc, n in zip(hq, ("q", "k", "v", "do")):
+                st_[n].copy_(hsrc, non_blocking=True)
+
+        def copy_out(st_, hset):
+            for n, hdst in zip(("o", "lse", "dq", "dk", "dv"), hset):
+                hdst.copy_(st_[n], non_blocking=True)
+
+        def serial_step():
+            copy_in(sets[0])
+            run_step(sets[0], sp)
+            copy_out(sets[0], hout[0])
+
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        freed = [torch.cuda.Event() for _ in range(2)]
+
+        def pipelined(n_steps):
+            for i in range(n_steps):
+                b_ = i % 2
+                with torch.cuda.stream(s_in):
+                    if i >= 2:
+                        s_in.wait_event(freed[b_])  # step i-2's results have left this set
+                    copy_in(sets[b_])
+                    in_ready[b_].record(s_in)
+                stream.wait_event(in_ready[b_])
+                run_step(sets[b_], sp)
+                done[b_].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(done[b_])
+                    copy_out(sets[b_], hout[b_])
+                    freed[b_].record(s_out)
+            stream.wait_stream(s_in)
+            stream.wait_stream(s_out)
 
         for _ in range(2):
-            e2e_step()
+            serial_step()
+        pipelined(2)
         torch.cuda.synchronize()
         ev0.record(stream)
         for _ in range(args.steps):
-            e2e_step()
+            serial_step()
         ev1.record(stream)
         torch.cuda.synchronize()
-        ms_e2e = max_over_ranks(ev0.elapsed_time(ev1), world)
-        e2e = {"value": whole_job_value(step_flops, args.steps, world, ms_e2e), "unit": "TFLOP/s",
+        ms_serial = max_over_ranks(ev0.elapsed_time(ev1), world)
+        s_in.wait_stream(stream)
+        ev0.record(s_in)
+        pipelined(args.steps)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms_pipe = max_over_ranks(ev0.elapsed_time(ev1), world)
+        assert binding.attn_check(sp) == 0
+        e2e = {"value": whole_job_value(step_flops, args.steps, world, ms_pipe), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": ms_e2e / args.steps}
+               "ms_per_step": ms_pipe / args.steps,
+               "mode": "pipelined: double-buffered device sets, copies on their own streams",
+               "serial": {"value": whole_job_value(step_flops, args.steps, world, ms_serial),
+                          "ms_per_step": ms_serial / args.steps}}
 
     if rank == 0:
         cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline_sample()
