@@ -135,15 +135,15 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def traffic_for(kernel):
+def traffic_for(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+    on the current kernel source and this workload; else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f).get(kernel)
-    if not rec:
+    if not rec or rec.get("workload") != workload:
         return None
     src = os.path.join(ROOT, "exact_attention_15_gb300", "csrc", rec["source"])
     with open(src, "rb") as f:
@@ -232,37 +232,49 @@ def main():
     w = W.WORKLOADS[name]
     if args.batch is not None and w.varlen is None:
         inp = W.custom(args.batch, w.H_q, w.H_kv, w.N, w.N, w.d, w.scale, w.causal, seed=w.seed,
-                       boost_frac=w.boost_frac, boost=w.boost)
-        w = W.Workload(w.name, args.batch, w.H_q, w.H_kv, w.N, w.d, w.scale, w.causal, w.seed)
+                       boost_frac=w.boost_frac, boost=w.boost, d_v=w.d_v)
+        w = W.Workload(w.name, args.batch, w.H_q, w.H_kv, w.N, w.d, w.scale, w.causal, w.seed,
+                       d_v=w.d_v)
     else:
         inp = W.generate(w.name)
+    # separate query/key and value head dimensions: the library has the forward
+    # pass only, so a step is one forward pass
+    fwd_only = inp.d_v != inp.d
     dev = lambda bits: torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
     q, k, v, do = dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.do)
     varlen = inp.cu_seqlens is not None
-    B, H, H_kv, d = inp.B, inp.H_q, inp.H_kv, inp.d
+    B, H, H_kv, d, d_v = inp.B, inp.H_q, inp.H_kv, inp.d, inp.d_v
     N = inp.N_q
     cu = torch.from_numpy(inp.cu_seqlens).cuda() if varlen else None
     cu_ptr = cu.data_ptr() if varlen else None
-    o = torch.empty_like(q)
+    o = torch.empty(q.shape[:-1] + (d_v,), dtype=q.dtype, device="cuda")
     lse = torch.empty((H, N) if varlen else (B, H, N), dtype=torch.float32, device="cuda")
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws_bytes = binding.attn_bwd_workspace_bytes(B, H, H_kv, N, N, d, varlen, 0)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    if fwd_only:
+        dq = dk = dv = None
+        ws_bytes, ws = 0, None
+    else:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws_bytes = binding.attn_bwd_workspace_bytes(B, H, H_kv, N, N, d, varlen, 0)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
 
     def step():
-        st = binding.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                              B, H, H_kv, N, N, d, w.causal, cu_ptr, w.scale, sp)
+        st = binding.attn_fwd_dims(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, H, H_kv, N, N, d, d_v, w.causal, cu_ptr,
+                                   w.scale, sp)
         assert st == 0, st
+        if fwd_only:
+            return
         st = binding.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                               do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                               B, H, H_kv, N, N, d, w.causal, cu_ptr, w.scale, 0, ws.data_ptr(),
                               ws_bytes, sp)
         assert st == 0, st
 
-    fwd_flops = W.fwd_flops(B, H, N, N, d, w.causal, seqlens=inp.seqlens() if varlen else None)
-    step_flops = fwd_flops * 3.5  # forward + 2.5x backward
+    fwd_flops = W.fwd_flops(B, H, N, N, d, w.causal, seqlens=inp.seqlens() if varlen else None,
+                            d_v=d_v)
+    step_flops = fwd_flops * (1.0 if fwd_only else 3.5)  # forward + 2.5x backward
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -308,7 +320,7 @@ def main():
         if kernel not in kt:
             return None
         ach = flops_per_launch / (kt[kernel]["avg_ms"] * 1e-3) / 1e12
-        tr = traffic_for(kernel)
+        tr = traffic_for(kernel, w.name if args.batch is None else None)
         return {"bound": "tensor", "achieved": ach, "peak": sustained, "unit": "TFLOP/s",
                 "frac": ach / sustained, "traffic": tr, "kernel": kernel,
                 "peak_kind": f"bf16_tflops_sustained ({peak_src})",
@@ -327,19 +339,26 @@ def main():
     # computes).
     e2e = None
     if not args.no_e2e:
-        hq = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (inp.q, inp.k, inp.v, inp.do)]
-        hout = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (o, lse, dq, dk, dv)]
+        names_in = ("q", "k", "v") if fwd_only else ("q", "k", "v", "do")
+        names_out = ("o", "lse") if fwd_only else ("o", "lse", "dq", "dk", "dv")
+        host_in = dict(q=inp.q, k=inp.k, v=inp.v, do=inp.do)
+        hq = [torch.from_numpy(host_in[n].view(np.int16)).view(torch.bfloat16).pin_memory()
+              for n in names_in]
+        sets = [dict(q=q, k=k, v=v, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv)]
+        sets[0] = {n: t for n, t in sets[0].items() if t is not None}
+        sets.append({n: torch.empty_like(t) for n, t in sets[0].items()})
+        hout = [[torch.empty(sets[0][n].shape, dtype=sets[0][n].dtype).pin_memory() for n in names_out]
                 for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in hq)
         d2h = sum(t.numel() * t.element_size() for t in hout[0])
-        sets = [dict(q=q, k=k, v=v, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv)]
-        sets.append({n: torch.empty_like(t) for n, t in sets[0].items()})
 
         def run_step(st_, sp_):
-            r = binding.attn_fwd(st_["q"].data_ptr(), st_["k"].data_ptr(), st_["v"].data_ptr(),
-                                 st_["o"].data_ptr(), st_["lse"].data_ptr(), B, H, H_kv, N, N, d,
-                                 w.causal, cu_ptr, w.scale, sp_)
+            r = binding.attn_fwd_dims(st_["q"].data_ptr(), st_["k"].data_ptr(), st_["v"].data_ptr(),
+                                      st_["o"].data_ptr(), st_["lse"].data_ptr(), B, H, H_kv, N, N,
+                                      d, d_v, w.causal, cu_ptr, w.scale, sp_)
             assert r == 0, r
+            if fwd_only:
+                return
             r = binding.attn_bwd(st_["q"].data_ptr(), st_["k"].data_ptr(), st_["v"].data_ptr(),
                                  st_["o"].data_ptr(), st_["lse"].data_ptr(), st_["do"].data_ptr(),
                                  st_["dq"].data_ptr(), st_["dk"].data_ptr(), st_["dv"].data_ptr(),
@@ -348,11 +367,11 @@ def main():
             assert r == 0, r
 
         def copy_in(st_):
-            for hsrc, n in zip(hq, ("q", "k", "v", "do")):
+            for hsrc, n in zip(hq, names_in):
                 st_[n].copy_(hsrc, non_blocking=True)
 
         def copy_out(st_, hset):
-            for n, hdst in zip(("o", "lse", "dq", "dk", "dv"), hset):
+            for n, hdst in zip(names_out, hset):
                 hdst.copy_(st_[n], non_blocking=True)
 
         def serial_step():
@@ -411,13 +430,15 @@ def main():
         cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline_sample()
         fwd_ms = kt.get("attn_fwd_kernel", {}).get("avg_ms")
         line = {
-            "metric": "attention fwd+bwd TFLOP/s (bf16, 1xGB300)", "value": value, "unit": "TFLOP/s",
+            "metric": ("attention fwd TFLOP/s (bf16, 1xGB300)" if fwd_only
+                       else "attention fwd+bwd TFLOP/s (bf16, 1xGB300)"), "value": value, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": f"{w.name}: " + (w.note or f"B{B} H{H} N{N} d{d}") + ", fwd+bwd",
+            "config": {"workload": f"{w.name}: " + (w.note or f"B{B} H{H} N{N} d{d}") +
+                                   (", fwd only" if fwd_only else ", fwd+bwd"),
                        "global_batch": B * world, "seq_len": N, "heads": H, "kv_heads": H_kv,
-                       "head_dim": d,
+                       "head_dim": d, "head_dim_v": d_v,
                        "parallelism": f"replicas x{world}",
                        "l2": f"inputs larger than L2 (q, k, v, o, dO: {q.numel() * 2 / 2**20:.0f} MiB each)"
                              if q.numel() * 2 * 5 > 129e6 else "inputs smaller than L2 (L2 not flushed)"},

@@ -30,6 +30,7 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SIGS = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, ctypes.c_float, _P]),
+    "attn_fwd_dims": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, ctypes.c_float, _P]),
     "attn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
                       ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
@@ -92,6 +93,12 @@ def exported_symbols():
 def attn_fwd(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, causal, seqlens, scale, stream) -> int:
     return load().attn_fwd(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, int(causal), seqlens,
                            float(scale), stream)
+
+
+def attn_fwd_dims(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d_qk, d_v, causal, seqlens, scale,
+                  stream) -> int:
+    return load().attn_fwd_dims(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d_qk, d_v, int(causal),
+                                seqlens, float(scale), stream)
 
 
 def attn_bwd_workspace_bytes(B, H_q, H_kv, N_q, N_k, d, varlen, deterministic) -> int:
@@ -178,8 +185,9 @@ def _check(status, what):
 
 
 def forward(q, k, v, scale=None, causal=False, cu_seqlens=None, out=None, lse=None):
-    """q [B, N_q, H_q, d] (or packed [T, H_q, d] with cu_seqlens), k/v likewise,
-    bf16 CUDA tensors. Returns (o, lse)."""
+    """q [B, N_q, H_q, d_qk] (or packed [T, H_q, d_qk] with cu_seqlens), k with
+    d_qk and v with d_v columns, bf16 CUDA tensors. Returns (o [.., d_v], lse).
+    The default scale is 1/sqrt(d_qk)."""
     import torch
     B, H_q, H_kv, N_q, N_k, d = _shape(q, k, cu_seqlens)
     if scale is None:
@@ -192,8 +200,10 @@ def forward(q, k, v, scale=None, causal=False, cu_seqlens=None, out=None, lse=No
         lse = torch.empty((H_q, N_q) if cu_seqlens is not None else (B, H_q, N_q),
                           dtype=torch.float32, device=q.device)
     cu_ptr = cu_seqlens.data_ptr() if cu_seqlens is not None else None
-    _check(attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                    B, H_q, H_kv, N_q, N_k, d, causal, cu_ptr, scale, _stream_ptr()), "attn_fwd")
+    d_v = v.shape[-1]
+    _check(attn_fwd_dims(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                         B, H_q, H_kv, N_q, N_k, d, d_v, causal, cu_ptr, scale, _stream_ptr()),
+           "attn_fwd_dims")
     return o, lse
 
 

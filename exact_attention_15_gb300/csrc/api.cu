@@ -17,7 +17,7 @@
 #include "attn_common.cuh"
 
 namespace attn {
-cudaError_t launch_attn_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+cudaError_t launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const FwdParams& p, dim3 grid,
                             cudaStream_t stream);
 cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int H_q, int* seq_order,
@@ -145,21 +145,23 @@ int plan_buffer(int dev, cudaStream_t stream, int seqs, PlanBuf* out) {
 // hardware block scheduler balance unequal tiles greedily. Equal tiles (fixed
 // length, no mask) always go persistent; otherwise persistence wins when the
 // start-up it saves per SM outweighs the imbalance static striding can leave,
-// at most about one longest tile (its key tiles times about 1.7 us at d = 128,
-// 0.9 us at d = 64, measured on GB300). Packed inputs use the mean length.
-bool fwd_persistent(long long tiles, int n_sm, bool causal, bool varlen, long long len, int d) {
+// at most about one longest tile (its key tiles times about 1.7 us at
+// d_qk = d_v = 128, scaled by d_qk + d_v above that, and 0.9 us at 64, measured
+// on GB300). Packed inputs use the mean length. `width` is d_qk + d_v.
+bool fwd_persistent(long long tiles, int n_sm, bool causal, bool varlen, long long len, int width) {
   if (!causal && !varlen) return true;
   const double saved_us = 2.0 * static_cast<double>(tiles) / n_sm;
-  const double longest_us = static_cast<double>((len + 127) / 128) * (d == 128 ? 1.7 : 0.9);
+  const double per_key_tile_us = width <= 128 ? 0.9 : 1.7 * width / 256.0;
+  const double longest_us = static_cast<double>((len + 127) / 128) * per_key_tile_us;
   return saved_us >= longest_us;
 }
 
 // Query heads per L2 section of the forward work list: as many whole KV-head
-// groups as keep their K and V (rows x d bf16 each) within a share of L2, cut
-// evenly over the KV heads.
-int l2_section_heads(int H_q, int H_kv, long long rows, int d) {
+// groups as keep their K and V (rows x (d_qk + d_v) bf16 values) within a share
+// of L2, cut evenly over the KV heads. `width` is d_qk + d_v.
+int l2_section_heads(int H_q, int H_kv, long long rows, int width) {
   constexpr long long kBudget = 48ll << 20;
-  const long long per_kv = 2ll * rows * d * 2;
+  const long long per_kv = rows * width * 2;
   long long fit = per_kv > 0 ? kBudget / per_kv : H_kv;
   if (fit < 1) fit = 1;
   if (fit > H_kv) fit = H_kv;
@@ -344,9 +346,21 @@ long long attn_set_wait_limit(long long cycles) {
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H_q,
              int H_kv, int N_q, int N_k, int d, int causal, const int* seqlens, float scale,
              attn_stream_t stream) {
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED_HEADDIM;
+  return attn_fwd_dims(q, k, v, o, lse, B, H_q, H_kv, N_q, N_k, d, d, causal, seqlens, scale,
+                       stream);
+}
+
+int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                  int H_q, int H_kv, int N_q, int N_k, int d_qk, int d_v, int causal,
+                  const int* seqlens, float scale, attn_stream_t stream) {
+  if (!((d_qk == 64 && d_v == 64) || (d_qk == 128 && d_v == 128) || (d_qk == 192 && d_v == 128)))
+    return ATTN_ERR_UNSUPPORTED_HEADDIM;
   Shape s;
-  int st = check_shape(B, H_q, H_kv, N_q, N_k, d, causal, seqlens, &s);
+  int st = check_shape(B, H_q, H_kv, N_q, N_k, d_v, causal, seqlens, &s);
   if (st != ATTN_OK) return st;
+  // element-count bound of check_shape, with the wider head dimension
+  if (static_cast<long long>(B) * (N_q + N_k) * H_q * d_qk > (1ll << 46)) return ATTN_ERR_BAD_SHAPE;
   // an empty tensor may come with a null pointer
   const bool has_q = B > 0 && N_q > 0, has_k = B > 0 && N_k > 0;
   if ((has_q && (!q || !o || !lse)) || (has_k && (!k || !v))) return ATTN_ERR_NULL_PTR;
@@ -363,11 +377,11 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   CUtensorMap tq, tk, tv;
   // with no keys at all nothing is ever loaded from k/v; map q instead of an empty extent
   const bool no_keys = (N_k == 0);
-  if (encode_rows_map(&tq, q, d, H_q, s.q_rows, s.q_batch) != ATTN_OK ||
-      encode_rows_map(&tk, no_keys ? q : k, d, no_keys ? H_q : H_kv, no_keys ? s.q_rows : s.k_rows,
-                      s.q_batch) != ATTN_OK ||
-      encode_rows_map(&tv, no_keys ? q : v, d, no_keys ? H_q : H_kv, no_keys ? s.q_rows : s.k_rows,
-                      s.q_batch) != ATTN_OK)
+  if (encode_rows_map(&tq, q, d_qk, H_q, s.q_rows, s.q_batch) != ATTN_OK ||
+      encode_rows_map(&tk, no_keys ? q : k, d_qk, no_keys ? H_q : H_kv,
+                      no_keys ? s.q_rows : s.k_rows, s.q_batch) != ATTN_OK ||
+      encode_rows_map(&tv, no_keys ? q : v, d_v, no_keys ? H_q : H_kv,
+                      no_keys ? s.q_rows : s.k_rows, s.q_batch) != ATTN_OK)
     return ATTN_ERR_CUDA;
 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
@@ -393,7 +407,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.total_tiles = static_cast<int>(tiles);
   p.n_mblocks = (N_q + 255) / 256;
   // the mean sequence length sizes the L2 sections of packed inputs
-  p.sec_heads = l2_section_heads(H_q, H_kv, seqlens ? (N_k + B - 1) / B : N_k, d);
+  p.sec_heads = l2_section_heads(H_q, H_kv, seqlens ? (N_k + B - 1) / B : N_k, d_qk + d_v);
   if (seqlens) {
     PlanBuf pb;
     if ((st = plan_buffer(dev, cs, B, &pb)) != ATTN_OK) return st;
@@ -408,10 +422,11 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (n_sm <= 0) return ATTN_ERR_CUDA;
   long long grid_x = tiles;
   if (fwd_persistent(tiles, n_sm, causal != 0, seqlens != nullptr,
-                     seqlens ? (N_k + B - 1) / B : N_k, d) &&
+                     seqlens ? (N_k + B - 1) / B : N_k, d_qk + d_v) &&
       grid_x > n_sm)
     grid_x = n_sm;
-  if (launch_attn_fwd(d, tq, tk, tv, p, dim3(static_cast<unsigned>(grid_x)), cs) != cudaSuccess)
+  if (launch_attn_fwd(d_qk, d_v, tq, tk, tv, p, dim3(static_cast<unsigned>(grid_x)), cs) !=
+      cudaSuccess)
     return ATTN_ERR_CUDA;
   return ATTN_OK;
 }

@@ -35,18 +35,33 @@
 
 namespace attn {
 
-template <int D>
+// Shared-memory plan. Q/K rows have DQK columns, V/O rows DV columns; every
+// tile is stored as 128-row x 64-column (16 KB) 128-byte-swizzled blocks.
+// Equal head dimensions: K and V share a ring of single-tile stages (load order
+// K0 V0 K1 V1 ...). DQK != DV (192 / 128): K and V tiles differ in size, and
+// two Q tiles plus stages of the larger tile do not fit, so the ring is made of
+// 16 KB block slots instead: K_j takes DQK / 64 consecutive slots, V_j DV / 64.
+template <int DQK, int DV>
 struct FwdCfg {
-  static constexpr int kHalves = D / 64;                 // 128-byte column blocks per row
-  static constexpr int kTileBytes = kTileM * D * 2;      // one 128-row bf16 tile
-  static constexpr int kStages = (D == 128) ? 4 : 8;     // K/V ring, one tile per stage
+  static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128, "head dimensions");
+  static constexpr int kQBlocks = DQK / 64;              // column blocks of a Q or K tile
+  static constexpr int kVBlocks = DV / 64;               // column blocks of a V tile
+  static constexpr int kBlockBytes = kTileM * 64 * 2;    // 16 KB
+  static constexpr int kQTileBytes = kQBlocks * kBlockBytes;
+  static constexpr bool kBlockRing = DQK != DV;
+  static constexpr int kTileBytes = kQTileBytes;         // one K or V stage (equal dims)
+  static constexpr int kStages = kBlockRing ? 1 : (DQK == 128 ? 4 : 8);
+  static constexpr int kSlots = 8;                       // block ring
+  static constexpr int kFullBars = 4;                    // block ring: loads in flight <= 8 / 2
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = 2 * kTileBytes;
-  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+  static constexpr int kKVOff = 2 * kQTileBytes;
+  static constexpr int kRingBytes = kBlockRing ? kSlots * kBlockBytes : kStages * kTileBytes;
+  static constexpr int kBarOff = kKVOff + kRingBytes;
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // barriers + alignment slack
-  static constexpr uint32_t kColO0 = 0, kColO1 = D;
-  static constexpr uint32_t kColS0 = 2 * D, kColS1 = 2 * D + 128;
+  static constexpr uint32_t kColO0 = 0, kColO1 = DV;
+  static constexpr uint32_t kColS0 = 2 * DV, kColS1 = 2 * DV + 128;
   static constexpr uint32_t kTmemCols = 512;
+  static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
 // Work decode: one work tile = two 128-row query tiles of one (batch, query head).
@@ -145,7 +160,7 @@ __device__ __forceinline__ bool next_tile(const FwdParams& p, int k, FwdTile& t)
 }
 
 // ------------------------------------------------------------------ softmax
-template <int D, int EMU, bool POS_SCALE>
+template <int EMU, bool POS_SCALE>
 __device__ __forceinline__ void softmax_row_tile(float (&s)[128], float c, float& m_used,
                                                  float& l, int kv0, int qrow, int Lk,
                                                  bool need_mask, int causal,
@@ -208,11 +223,11 @@ __device__ __forceinline__ void softmax_row_tile(float (&s)[128], float c, float
   l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
 }
 
-template <int D, int EMU>
+template <int DQK, int DV, int EMU>
 __global__ void __launch_bounds__(384, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using Cfg = FwdCfg<D>;
+  using Cfg = FwdCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -230,7 +245,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(smem_addr(&bars->p_full[i]), 128);
       mbar_init(smem_addr(&bars->pv_done[i]), 1);
     }
-    for (int i = 0; i < Cfg::kStages; ++i) {
+    // tile ring: kv_full / kv_empty per stage; block ring: kv_full per load in
+    // flight, kv_empty per slot
+    for (int i = 0; i < (Cfg::kBlockRing ? Cfg::kSlots : Cfg::kStages); ++i) {
       mbar_init(smem_addr(&bars->kv_full[i]), 1);
       mbar_init(smem_addr(&bars->kv_empty[i]), 1);
     }
@@ -260,8 +277,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      uint32_t ld = 0;  // K/V loads issued so far (K_j, V_j of each tile in turn)
-      int qk = 0;       // tiles whose Q was loaded (tiles that see no key load nothing)
+      uint32_t ld = 0;   // K/V loads issued so far (K_j, V_j of each tile in turn)
+      uint32_t pos = 0;  // block ring: block slots filled so far
+      int qk = 0;        // tiles whose Q was loaded (tiles that see no key load nothing)
       FwdTile t;
       bool ok = true;
       for (int k = 0; ok && next_tile(p, k, t); ++k) {
@@ -276,31 +294,55 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           ++qk;
           const uint32_t qbar = smem_addr(&bars->q_full);
           const int nq = (t.n[0] > 0) + (t.n[1] > 0);
-          mbar_arrive_expect_tx(qbar, nq * Cfg::kTileBytes);
+          mbar_arrive_expect_tx(qbar, nq * Cfg::kQTileBytes);
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             if (t.n[i] == 0) continue;
-            const uint32_t dst = smem_addr(smem + Cfg::kQOff + i * Cfg::kTileBytes);
-            for (int hf = 0; hf < Cfg::kHalves; ++hf)
+            const uint32_t dst = smem_addr(smem + Cfg::kQOff + i * Cfg::kQTileBytes);
+            for (int hf = 0; hf < Cfg::kQBlocks; ++hf)
               tma_load_4d(dst + hf * 16384, &tm_q, qbar, hf * 64, t.h,
                           t.row_base + t.q0 + i * kTileM, t.batch_coord);
           }
           for (int it = 0; it < 2 * n_kv; ++it, ++ld) {
             const int j = it >> 1;
-            const uint32_t stage = ld % Cfg::kStages;
-            const uint32_t round = ld / Cfg::kStages;
-            if (!mbar_wait(smem_addr(&bars->kv_empty[stage]), (round & 1) ^ 1, lim)) {
-              record_error(p.err, kErrTimeout);
-              ok = false;
-              break;
-            }
-            const uint32_t fbar = smem_addr(&bars->kv_full[stage]);
-            mbar_arrive_expect_tx(fbar, Cfg::kTileBytes);
-            const uint32_t dst = smem_addr(smem + Cfg::kKVOff + stage * Cfg::kTileBytes);
             const CUtensorMap* map = (it & 1) ? &tm_v : &tm_k;
-            for (int hf = 0; hf < Cfg::kHalves; ++hf)
-              tma_load_4d(dst + hf * 16384, map, fbar, hf * 64, t.h_kv, t.row_base + j * kTileN,
-                          t.batch_coord);
+            if constexpr (!Cfg::kBlockRing) {
+              const uint32_t stage = ld % Cfg::kStages;
+              const uint32_t round = ld / Cfg::kStages;
+              if (!mbar_wait(smem_addr(&bars->kv_empty[stage]), (round & 1) ^ 1, lim)) {
+                record_error(p.err, kErrTimeout);
+                ok = false;
+                break;
+              }
+              const uint32_t fbar = smem_addr(&bars->kv_full[stage]);
+              mbar_arrive_expect_tx(fbar, Cfg::kTileBytes);
+              const uint32_t dst = smem_addr(smem + Cfg::kKVOff + stage * Cfg::kTileBytes);
+              for (int hf = 0; hf < Cfg::kQBlocks; ++hf)
+                tma_load_4d(dst + hf * 16384, map, fbar, hf * 64, t.h_kv, t.row_base + j * kTileN,
+                            t.batch_coord);
+            } else {
+              // block ring: the load's blocks go to slots pos, pos + 1, ... (mod 8).
+              // V is read as an MN-major operand whose two column blocks must be
+              // a fixed stride apart; when it wraps (slots 7 and 0) its first
+              // column block goes to slot 0 and its second to slot 7.
+              const int nb = (it & 1) ? Cfg::kVBlocks : Cfg::kQBlocks;
+              const uint32_t fbar = smem_addr(&bars->kv_full[ld % Cfg::kFullBars]);
+              mbar_arrive_expect_tx(fbar, nb * Cfg::kBlockBytes);
+              const bool wrap_v = (it & 1) && (pos % Cfg::kSlots) == Cfg::kSlots - 1;
+              for (int blk = 0; blk < nb; ++blk, ++pos) {
+                const uint32_t slot = pos % Cfg::kSlots;
+                if (!mbar_wait(smem_addr(&bars->kv_empty[slot]), ((pos / Cfg::kSlots) & 1) ^ 1,
+                               lim)) {
+                  record_error(p.err, kErrTimeout);
+                  ok = false;
+                  break;
+                }
+                const int col_blk = wrap_v ? (1 - blk) : blk;
+                tma_load_4d(smem_addr(smem + Cfg::kKVOff + slot * Cfg::kBlockBytes), map, fbar,
+                            col_blk * 64, t.h_kv, t.row_base + j * kTileN, t.batch_coord);
+              }
+              if (!ok) break;
+            }
           }
         }
       }
@@ -314,34 +356,84 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // time, so this thread does as little else as possible between MMAs.
     if (lane == 0) {
       constexpr uint32_t kIdS = make_idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t kIdPV = make_idesc_bf16(128, D, 0, 1);
+      constexpr uint32_t kIdPV = make_idesc_bf16(128, DV, 0, 1);
+      constexpr int kQB = Cfg::kQBlocks, kVB = Cfg::kVBlocks;
       const uint32_t q_base = smem_addr(smem + Cfg::kQOff);
       const uint32_t kv_base = smem_addr(smem + Cfg::kKVOff);
-      // Descriptors are built once; each MMA only adds a compile-time byte
-      // offset (>> 4) to the start-address field.
+      // Descriptors are built once; each MMA only adds a byte offset (>> 4) to
+      // the start-address field (compile-time for the tile ring).
       const uint64_t q_desc = make_sdesc_sw128(q_base, 16, 1024);     // K-major
       const uint64_t k_desc = make_sdesc_sw128(kv_base, 16, 1024);    // K-major
       const uint64_t v_desc = make_sdesc_sw128(kv_base, 16384, 1024); // MN-major
-      auto issue_s = [&](int i, uint32_t stage) {
-        const uint64_t qa = q_desc + ((i * Cfg::kTileBytes) >> 4);
-        const uint64_t kb = k_desc + ((stage * Cfg::kTileBytes) >> 4);
+      // block ring, V wrapped over the ring's end: first column block in slot 0,
+      // second in slot 7
+      const uint64_t v_desc_wrap = make_sdesc_sw128(kv_base, 7 * 16384, 1024);
+      uint32_t ld = 0;     // K/V loads consumed so far, in the producer's order
+      uint32_t pos = 0;    // block ring: block slots consumed so far
+      // Load `it` of the current tile (K_j = 2j, V_j = 2j + 1): its barrier, its
+      // phase, its place in shared memory.
+      auto stage_of = [&](int it) { return (ld + it) % Cfg::kStages; };
+      auto pos_of = [&](int it) { return pos + (it >> 1) * (kQB + kVB) + ((it & 1) ? kQB : 0); };
+      auto full_bar = [&](int it) {
+        if constexpr (Cfg::kBlockRing) return smem_addr(&bars->kv_full[(ld + it) % Cfg::kFullBars]);
+        else return smem_addr(&bars->kv_full[stage_of(it)]);
+      };
+      auto full_phase = [&](int it) -> uint32_t {
+        if constexpr (Cfg::kBlockRing) return ((ld + it) / Cfg::kFullBars) & 1;
+        else return ((ld + it) / Cfg::kStages) & 1;
+      };
+      auto release = [&](int it) {  // the load's buffer is free once the MMAs so far are done
+        if constexpr (Cfg::kBlockRing) {
+          const uint32_t p0 = pos_of(it);
+          const int nb = (it & 1) ? kVB : kQB;
+          for (int b = 0; b < nb; ++b) mma_commit(smem_addr(&bars->kv_empty[(p0 + b) % Cfg::kSlots]));
+        } else {
+          mma_commit(smem_addr(&bars->kv_empty[stage_of(it)]));
+        }
+      };
+      auto issue_s = [&](int i, int it) {
+        uint64_t qa = q_desc + ((i * Cfg::kQTileBytes) >> 4);
+        // With 12 K steps per S the compiler would keep every Q descriptor of
+        // both tiles live across the loop and spill; an opaque copy makes it
+        // add the offsets at each issue instead.
+        if constexpr (Cfg::kBlockRing) asm volatile("" : "+l"(qa));
         const uint32_t d_tmem = tmem + Cfg::kColS0 + i * 128;
+        if constexpr (Cfg::kBlockRing) {
+          const uint32_t p0 = pos_of(it);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          mma_ss(d_tmem, qa + off, kb + off, kIdS, kk > 0);
+          for (int b = 0; b < kQB; ++b) {
+            const uint64_t kb = k_desc + ((((p0 + b) % Cfg::kSlots) * 16384) >> 4);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const int kk = 4 * b + k4;
+              const uint32_t qoff = (b * 16384 + k4 * 32) >> 4;
+              mma_ss(d_tmem, qa + qoff, kb + ((k4 * 32) >> 4), kIdS, kk > 0);
+            }
+          }
+        } else {
+          const uint64_t kb = k_desc + ((stage_of(it) * Cfg::kTileBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < DQK / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+            mma_ss(d_tmem, qa + off, kb + off, kIdS, kk > 0);
+          }
         }
         mma_commit(smem_addr(&bars->s_full[i]));
       };
-      auto issue_pv = [&](int i, uint32_t stage, bool acc) {
-        const uint64_t vb = v_desc + ((stage * Cfg::kTileBytes) >> 4);
-        const uint32_t d_tmem = tmem + Cfg::kColO0 + i * D;
+      auto issue_pv = [&](int i, int it, bool acc) {
+        uint64_t vb;
+        if constexpr (Cfg::kBlockRing) {
+          const uint32_t slot = pos_of(it) % Cfg::kSlots;
+          vb = (slot == Cfg::kSlots - 1) ? v_desc_wrap : v_desc + ((slot * 16384) >> 4);
+        } else {
+          vb = v_desc + ((stage_of(it) * Cfg::kTileBytes) >> 4);
+        }
+        const uint32_t d_tmem = tmem + Cfg::kColO0 + i * DV;
         const uint32_t a_tmem = tmem + Cfg::kColS0 + i * 128;
 #pragma unroll
         for (int kk = 0; kk < kTileN / 16; ++kk)
           mma_ts(d_tmem, a_tmem + kk * 8, vb + kk * (2048 >> 4), kIdPV, (acc || kk > 0));
       };
-      uint32_t ld = 0;     // K/V loads consumed so far, in the producer's order
       int pw[2] = {0, 0};  // p_full waits so far, per query tile
       int qk = 0;          // tiles with a Q load
       bool ok = true;
@@ -349,25 +441,27 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int k = 0; ok && next_tile(p, k, t); ++k) {
         const int n_kv = max(t.n[0], t.n[1]);
         if (n_kv == 0) continue;  // no keys: the epilogue writes O = 0, LSE = -inf
-        // K_j is load ld + 2j, V_j load ld + 2j + 1
-        auto stage_of = [&](int it) { return (ld + it) % Cfg::kStages; };
-        auto phase_of = [&](int it) { return ((ld + it) / Cfg::kStages) & 1; };
         ok = mbar_wait(smem_addr(&bars->q_full), qk & 1, lim);
         ++qk;
-        if (ok) ok = mbar_wait(smem_addr(&bars->kv_full[stage_of(0)]), phase_of(0), lim);
+        if (ok) ok = mbar_wait(full_bar(0), full_phase(0), lim);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int i = 0; i < 2; ++i)
-          if (t.n[i] > 0) issue_s(i, stage_of(0));
-        mma_commit(smem_addr(&bars->kv_empty[stage_of(0)]));
+          if (t.n[i] > 0) issue_s(i, 0);
+        release(0);
         // Q is free again once the tile's last S MMA is done
         if (n_kv == 1) mma_commit(smem_addr(&bars->q_empty));
         for (int j = 0; j < n_kv; ++j) {
           const int itv = 2 * j + 1, itk = 2 * j + 2;
           const bool next_k = (j + 1) < n_kv;
-          ok = mbar_wait(smem_addr(&bars->kv_full[stage_of(itv)]), phase_of(itv), lim);
-          if (ok && next_k) ok = mbar_wait(smem_addr(&bars->kv_full[stage_of(itk)]), phase_of(itk), lim);
+          // Block ring (shallow: about 1.6 key/value steps fit): K_{j+1} is waited
+          // for only before the first S MMA that reads it, and V_j's slots are
+          // released right after its last PV MMA, which gives the producer the
+          // earliest start on the following loads.
+          bool k_ready = !Cfg::kBlockRing || !next_k;
+          ok = mbar_wait(full_bar(itv), full_phase(itv), lim);
+          if (ok && next_k && !Cfg::kBlockRing) ok = mbar_wait(full_bar(itk), full_phase(itk), lim);
           if (!ok) break;
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
@@ -375,18 +469,29 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!mbar_wait(smem_addr(&bars->p_full[i]), pw[i] & 1, lim)) { ok = false; break; }
             ++pw[i];
             tc_fence_after();
-            issue_pv(i, stage_of(itv), j > 0);
+            issue_pv(i, itv, j > 0);
+            if constexpr (Cfg::kBlockRing) {
+              if (i == 1 || j >= t.n[1]) release(itv);  // the last PV reading V_j
+            }
             // only the last PV of a tile is signalled (to the epilogue); earlier
             // ones are covered by the commit of the S MMA issued after them
-            if (j + 1 == t.n[i]) mma_commit(smem_addr(&bars->pv_done[i]));
-            else issue_s(i, stage_of(itk));
+            if (j + 1 == t.n[i]) {
+              mma_commit(smem_addr(&bars->pv_done[i]));
+            } else {
+              if (!k_ready) {
+                if (!(ok = mbar_wait(full_bar(itk), full_phase(itk), lim))) break;
+                k_ready = true;
+              }
+              issue_s(i, itk);
+            }
           }
           if (!ok) break;
-          mma_commit(smem_addr(&bars->kv_empty[stage_of(itv)]));
-          if (next_k) mma_commit(smem_addr(&bars->kv_empty[stage_of(itk)]));
+          if (!Cfg::kBlockRing) release(itv);
+          if (next_k) release(itk);
           if (j + 2 == n_kv) mma_commit(smem_addr(&bars->q_empty));
         }
         ld += 2 * n_kv;
+        pos += n_kv * (kQB + kVB);
       }
       if (!ok) record_error(p.err, kErrTimeout);
     }
@@ -432,16 +537,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bool rescale_warp;
         float factor;
         if (c > 0.0f)
-          softmax_row_tile<D, EMU, true>(s, c, m_used, l, kv0, qrow, Lk, need_mask, p.causal, pk,
+          softmax_row_tile<EMU, true>(s, c, m_used, l, kv0, qrow, Lk, need_mask, p.causal, pk,
                                          rescale_warp, factor);
         else
-          softmax_row_tile<D, 0, false>(s, c, m_used, l, kv0, qrow, Lk, need_mask, p.causal, pk,
+          softmax_row_tile<0, false>(s, c, m_used, l, kv0, qrow, Lk, need_mask, p.causal, pk,
                                         rescale_warp, factor);
         if (rescale_warp && j > 0 && __any_sync(0xffffffffu, factor != 1.0f)) {
           // correction: O_{j-1} is complete here, because the commit that
           // signalled S_j came from the thread that issued PV_{j-1} before S_j
 #pragma unroll
-          for (int cc = 0; cc < D / 32; ++cc) {
+          for (int cc = 0; cc < DV / 32; ++cc) {
             uint32_t ov[32];
             tmem_ld32(tmem + lane_base + col_o + cc * 32, ov);
             tmem_ld_wait(ov);
@@ -472,11 +577,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
         const size_t grow = static_cast<size_t>(t.row_base) + qrow;  // packed row
         const size_t o_off =
-            p.cu_seqlens ? (grow * p.H_q + t.h) * D
-                         : ((static_cast<size_t>(t.b) * p.N_q + qrow) * p.H_q + t.h) * D;
+            p.cu_seqlens ? (grow * p.H_q + t.h) * DV
+                         : ((static_cast<size_t>(t.b) * p.N_q + qrow) * p.H_q + t.h) * DV;
         uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + o_off);
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < DV / 32; ++cc) {
           uint32_t ov[32];
           if (have_o) {
             tmem_ld32(tmem + lane_base + col_o + cc * 32, ov);
@@ -584,12 +689,12 @@ fwd_plan_kernel(const int* __restrict__ cu_seqlens, int B, int H_q, int sort, in
 
 // ------------------------------------------------------------------ host side
 
-template <int D, int EMU>
+template <int DQK, int DV, int EMU>
 static cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tv, const FwdParams& p, dim3 grid,
                                    cudaStream_t stream) {
-  using Cfg = FwdCfg<D>;
-  auto kern = attn_fwd_kernel<D, EMU>;
+  using Cfg = FwdCfg<DQK, DV>;
+  auto kern = attn_fwd_kernel<DQK, DV, EMU>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -606,11 +711,14 @@ static cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk,
 #define ATTN_FWD_EMU 0
 #endif
 
-cudaError_t launch_attn_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+// Supported (d_qk, d_v): (64, 64), (128, 128), (192, 128); the caller checks.
+cudaError_t launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const FwdParams& p, dim3 grid,
                             cudaStream_t stream) {
-  if (d == 64) return launch_fwd_impl<64, ATTN_FWD_EMU>(tq, tk, tv, p, grid, stream);
-  return launch_fwd_impl<128, ATTN_FWD_EMU>(tq, tk, tv, p, grid, stream);
+  if (d_qk == 64 && d_v == 64) return launch_fwd_impl<64, 64, ATTN_FWD_EMU>(tq, tk, tv, p, grid, stream);
+  if (d_qk == 192 && d_v == 128)
+    return launch_fwd_impl<192, 128, ATTN_FWD_EMU>(tq, tk, tv, p, grid, stream);
+  return launch_fwd_impl<128, 128, ATTN_FWD_EMU>(tq, tk, tv, p, grid, stream);
 }
 
 // Largest packed batch the plan kernel sorts (its lengths and order sit in

@@ -50,6 +50,7 @@ class Workload:
     boost_frac: float = 0.0    # fraction of key rows scaled before rounding
     boost: float = 1.0
     note: str = ""
+    d_v: int = None            # value / output head dimension (None: same as d)
 
 
 WORKLOADS = {
@@ -66,6 +67,12 @@ WORKLOADS = {
     "long": Workload("long", 1, 16, 16, 32768, 128, 1.0 / math.sqrt(128.0), True, 1004,
                      boost_frac=0.05, boost=3.0,
                      note="B1 H16 N32768 d128 causal, 5% of key rows x3"),
+    # forward only: the (192, 128) head dimensions of the DeepSeek V3 architecture
+    # that the FlashAttention-4 benchmark also runs (16 heads, 32k tokens)
+    "mla": Workload("mla", 4, 16, 16, 8192, 192, 1.0 / math.sqrt(192.0), False, 1006,
+                    note="B4 H16 N8192 d_qk 192 d_v 128, non-causal", d_v=128),
+    "mla_causal": Workload("mla_causal", 4, 16, 16, 8192, 192, 1.0 / math.sqrt(192.0), True, 1006,
+                           note="B4 H16 N8192 d_qk 192 d_v 128, causal", d_v=128),
     "varlen_gqa": Workload("varlen_gqa", 16, 32, 8, 4096, 128, 1.0 / math.sqrt(128.0), True, 1005,
                            varlen=(16, 512, 4096),
                            note="16 packed sequences, lengths U[512,4096], H_q 32 / H_kv 8, causal"),
@@ -91,8 +98,9 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
 class Inputs:
     """Raw bf16 bits plus the shape description.
 
-    Fixed length: q/do [B, N, H_q, d], k/v [B, N, H_kv, d].
-    Packed: q/do [T, H_q, d], k/v [T, H_kv, d], cu_seqlens int32 [n_seqs + 1]."""
+    Fixed length: q [B, N, H_q, d], k [B, N, H_kv, d], v [B, N, H_kv, d_v],
+    do [B, N, H_q, d_v]. Packed: the same without B and with T rows,
+    cu_seqlens int32 [n_seqs + 1]. ``d_v`` defaults to ``d``."""
     q: np.ndarray
     k: np.ndarray
     v: np.ndarray
@@ -107,6 +115,11 @@ class Inputs:
     causal: bool
     cu_seqlens: np.ndarray = None
     meta: dict = field(default_factory=dict)
+    d_v: int = None
+
+    def __post_init__(self):
+        if self.d_v is None:
+            self.d_v = self.d
 
     @property
     def varlen(self) -> bool:
@@ -123,9 +136,12 @@ def _normal_bits(rng, shape):
 
 
 def custom(B, H_q, H_kv, N_q, N_k, d, scale=None, causal=False, seed=7, seqlens=None,
-           boost_frac=0.0, boost=1.0, parts=("q", "k", "v", "do")) -> Inputs:
+           boost_frac=0.0, boost=1.0, parts=("q", "k", "v", "do"), d_v=None) -> Inputs:
     """General generator. ``seqlens`` (list of ints) selects packed layout; then
-    B = len(seqlens) and N_q = N_k = sum(seqlens)."""
+    B = len(seqlens) and N_q = N_k = sum(seqlens). ``d_v`` (default ``d``) is the
+    head dimension of v and dO."""
+    if d_v is None:
+        d_v = d
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -137,12 +153,14 @@ def custom(B, H_q, H_kv, N_q, N_k, d, scale=None, causal=False, seed=7, seqlens=
         cu[1:] = np.cumsum(seqlens)
         B = len(seqlens)
         N_q = N_k = int(cu[-1])
-        q_shape, kv_shape = (N_q, H_q, d), (N_k, H_kv, d)
+        lead_q, lead_k = (N_q,), (N_k,)
     else:
-        q_shape, kv_shape = (B, N_q, H_q, d), (B, N_k, H_kv, d)
+        lead_q, lead_k = (B, N_q), (B, N_k)
+    shapes = dict(q=lead_q + (H_q, d), k=lead_k + (H_kv, d), v=lead_k + (H_kv, d_v),
+                  do=lead_q + (H_q, d_v))
     out = {}
     for name in ("q", "k", "v", "do"):
-        shape = q_shape if name in ("q", "do") else kv_shape
+        shape = shapes[name]
         if name not in parts:
             out[name] = None
             # keep the stream aligned: draw and drop
@@ -164,7 +182,7 @@ def custom(B, H_q, H_kv, N_q, N_k, d, scale=None, causal=False, seed=7, seqlens=
         del x
     return Inputs(out["q"], out["k"], out["v"], out["do"], B, H_q, H_kv, N_q, N_k, d,
                   float(scale), bool(causal), cu,
-                  meta=dict(seed=seed, boost_frac=boost_frac, boost=boost))
+                  meta=dict(seed=seed, boost_frac=boost_frac, boost=boost), d_v=d_v)
 
 
 def generate(name: str, parts=("q", "k", "v", "do")) -> Inputs:
@@ -175,20 +193,23 @@ def generate(name: str, parts=("q", "k", "v", "do")) -> Inputs:
         rng2 = np.random.Generator(np.random.PCG64(w.seed + 7))
         seqlens = rng2.integers(lo, hi, size=n_seqs, endpoint=True)
         inp = custom(n_seqs, w.H_q, w.H_kv, 0, 0, w.d, w.scale, w.causal, seed=w.seed,
-                     seqlens=seqlens, parts=parts)
+                     seqlens=seqlens, parts=parts, d_v=w.d_v)
     else:
         inp = custom(w.B, w.H_q, w.H_kv, w.N, w.N, w.d, w.scale, w.causal, seed=w.seed,
-                     boost_frac=w.boost_frac, boost=w.boost, parts=parts)
+                     boost_frac=w.boost_frac, boost=w.boost, parts=parts, d_v=w.d_v)
     inp.meta["workload"] = name
     return inp
 
 
-def fwd_flops(B, H_q, N_q, N_k, d, causal, seqlens=None) -> float:
+def fwd_flops(B, H_q, N_q, N_k, d, causal, seqlens=None, d_v=None) -> float:
     """Convention of the FlashAttention-4 benchmark: 4 * N_q * N_k * d per head,
-    halved for causal; packed inputs use sum of L^2. Backward is 2.5x this."""
+    halved for causal; packed inputs use sum of L^2. Backward is 2.5x this. With
+    separate head dimensions the two contractions count 2 * N_q * N_k * d (QK^T)
+    and 2 * N_q * N_k * d_v (PV)."""
+    width = 2.0 * d if d_v is None else float(d + d_v)
     if seqlens is not None:
         pairs = float(sum(int(L) * int(L) for L in seqlens))
-        f = 4.0 * pairs * d * H_q
+        f = 2.0 * pairs * width * H_q
     else:
-        f = 4.0 * B * H_q * float(N_q) * float(N_k) * d
+        f = 2.0 * B * H_q * float(N_q) * float(N_k) * width
     return f / 2.0 if causal else f

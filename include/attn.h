@@ -65,7 +65,7 @@ typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_NULL_PTR = 1,             /* a required pointer is NULL */
   ATTN_ERR_ALIGNMENT = 2,            /* a tensor pointer is not 16-byte aligned */
-  ATTN_ERR_UNSUPPORTED_HEADDIM = 3,  /* d not in {64, 128} */
+  ATTN_ERR_UNSUPPORTED_HEADDIM = 3,  /* head dimensions not supported (see each call) */
   ATTN_ERR_BAD_SHAPE = 4,            /* a size is negative, too large, or inconsistent */
   ATTN_ERR_GQA_RATIO = 5,            /* H_q not a positive multiple of H_kv */
   ATTN_ERR_CAUSAL_SHAPE = 6,         /* causal with N_q != N_k (alignment undefined) */
@@ -95,6 +95,23 @@ typedef enum {
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H_q, int H_kv, int N_q, int N_k, int d, int causal,
              const int* seqlens, float scale, attn_stream_t stream);
+
+/*
+ * Forward pass with separate head dimensions for queries/keys (d_qk) and for
+ * values/outputs (d_v): S = scale * Q K^T contracts over d_qk, O = P V has d_v
+ * columns. The FlashAttention-4 summary (experimental setup) benchmarks the
+ * (192, 128) head dimensions of the DeepSeek V3 architecture besides equal ones.
+ * Supported pairs: (64, 64), (128, 128), (192, 128); anything else returns
+ * ATTN_ERR_UNSUPPORTED_HEADDIM. Layouts as for attn_fwd with d replaced by d_qk
+ * in q and k and by d_v in v and o: q [B, N_q, H_q, d_qk], k [B, N_k, H_kv, d_qk],
+ * v [B, N_k, H_kv, d_v], o [B, N_q, H_q, d_v] (packed: [T, H, d_*]). Everything
+ * else (lse, masks, packed inputs, errors, ownership, streams) is as for
+ * attn_fwd, which is this call with d_qk = d_v = d. attn_bwd supports only
+ * equal head dimensions.
+ */
+int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* lse,
+                  int B, int H_q, int H_kv, int N_q, int N_k, int d_qk, int d_v, int causal,
+                  const int* seqlens, float scale, attn_stream_t stream);
 
 /*
  * Bytes of device workspace attn_bwd needs for these sizes (0 on invalid

@@ -90,6 +90,29 @@ def test_bwd_argument_errors(lib, kw, code):
     assert _bwd(lib, **kw) == code
 
 
+def _fwd_dims(lib, d_qk, d_v, **kw):
+    a = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H_q=2, H_kv=2, N_q=128, N_k=128, causal=0,
+             seqlens=None, scale=0.125)
+    a.update(kw)
+    return lib.attn_fwd_dims(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H_q"], a["H_kv"],
+                             a["N_q"], a["N_k"], d_qk, d_v, a["causal"], a["seqlens"], a["scale"],
+                             None)
+
+
+@pytest.mark.parametrize("d_qk,d_v", [(192, 192), (128, 64), (64, 128), (192, 64), (256, 128),
+                                      (128, 192), (96, 96)])
+def test_fwd_dims_unsupported_pairs(lib, d_qk, d_v):
+    assert _fwd_dims(lib, d_qk, d_v) == 3
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H_q=3, H_kv=2), 5), (dict(causal=1, N_k=64), 6), (dict(v=None), 1), (dict(o=A + 8), 2),
+    (dict(scale=float("nan")), 4),
+])
+def test_fwd_dims_argument_errors(lib, kw, code):
+    assert _fwd_dims(lib, 192, 128, **kw) == code
+
+
 def test_empty_problems_need_no_pointers(lib):
     assert _fwd(lib, B=0, q=None, k=None, v=None, o=None, lse=None) == 0
     assert _bwd(lib, B=0, q=None, k=None, v=None, o=None, lse=None, do=None, dq=None, dk=None,
@@ -119,3 +142,4 @@ def test_no_device_is_reported():
     lib = binding.load()
     assert _fwd(lib) == 10
     assert _bwd(lib) == 10
+    assert _fwd_dims(lib, 192, 128) == 10

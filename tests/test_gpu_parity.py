@@ -140,6 +140,27 @@ def test_worked_example_on_gpu(d):
         assert abs(float(lse.cpu()[0, 0, 0]) - ref_lse) < 2e-3
 
 
+# d_qk = 192, d_v = 128 (forward only). Eight or more key tiles put a V tile
+# across the end of the block ring (its column blocks in slots 7 and 0).
+ASYM = {
+    "asym_ragged_causal": dict(B=2, H_q=2, H_kv=2, N_q=300, N_k=300, causal=True),
+    "asym_gqa_ring_wrap": dict(B=1, H_q=4, H_kv=2, N_q=1000, N_k=1000, causal=False),
+    "asym_gqa_ring_wrap_causal": dict(B=1, H_q=4, H_kv=2, N_q=1300, N_k=1300, causal=True),
+    "asym_cross_lengths": dict(B=2, H_q=1, H_kv=1, N_q=200, N_k=1333, causal=False),
+    "asym_varlen": dict(B=0, H_q=4, H_kv=1, N_q=0, N_k=0, causal=True,
+                        seqlens=[1, 127, 0, 129, 1100, 300, 64]),
+    "asym_no_keys_rows": dict(B=1, H_q=2, H_kv=1, N_q=5, N_k=700, causal=False),
+}
+
+
+@pytest.mark.parametrize("name", list(ASYM))
+def test_asymmetric_head_dims_forward(name):
+    inp = W.custom(seed=200 + len(name), d=192, d_v=128, parts=("q", "k", "v"), **ASYM[name])
+    o, lse, _ = run_forward(inp)
+    assert tuple(o.shape[-1:]) == (128,)
+    _oracle_fwd_check(inp, o, lse, _all_pairs(inp))
+
+
 def test_forward_on_concurrent_streams():
     """Forward passes issued on two streams at once (each stream has its own work
     counter) give the same bits as the same passes run one after the other, and
@@ -209,6 +230,8 @@ FULL = [
     ("mid_causal", 3, 512),
     ("long", 2, 384),
     ("varlen_gqa", 2, None),
+    ("mla", 3, 512),
+    ("mla_causal", 3, 512),
 ]
 
 

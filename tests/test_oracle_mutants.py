@@ -51,6 +51,8 @@ MUTANTS = [
     ("packed_sequences_overlap", ATT, "return [(s, (int(cu[s]), int(cu[s + 1]))) for s in range(len(cu) - 1)]",
      "return [(s, (int(cu[s]), int(cu[s + 1]) + (1 if s < len(cu) - 2 else 0))) for s in range(len(cu) - 1)]",
      ["check_packed_is_per_sequence"]),
+    ("o_from_keys", ATT, "o[r0:r0 + len(rr)] = p @ v", "o[r0:r0 + len(rr)] = p @ k[:, : v.shape[1]]",
+     ["check_asymmetric_head_dims", "check_brute_force_scalar"]),
     ("merge_rescales_denominator_only", ONL, "u = c * u + e @ vb", "u = u + e @ vb",
      ["check_online_merge", "check_merges_match_definition"]),
     ("merge_rescales_numerator_only", ONL, "l = c * l + float(np.sum(e))", "l = l + float(np.sum(e))",
@@ -83,7 +85,7 @@ def test_mutant_is_caught(mid, path, old, new, checks):
 def test_unmutated_oracle_passes_every_check():
     for name in ("check_worked_example_forward", "check_finite_differences", "check_brute_force_scalar",
                  "check_invariants", "check_closed_forms", "check_gqa_is_repeated_heads",
-                 "check_packed_is_per_sequence"):
+                 "check_packed_is_per_sequence", "check_asymmetric_head_dims"):
         getattr(P, name)(P.A)
     P.check_online_merge(P.OL)
     P.check_merges_match_definition(P.A, P.OL)

@@ -248,6 +248,29 @@ def test_closed_forms():
     check_closed_forms(A)
 
 
+def check_asymmetric_head_dims(att, seed=29):
+    """Queries/keys and values of different widths (the FlashAttention-4 benchmark
+    also runs d_qk = 192, d_v = 128; here 5 and 3): O has d_v columns and equals
+    the scalar textbook loop; scale 0 gives the mean of the V rows."""
+    rng = np.random.default_rng(seed)
+    for causal in (False, True):
+        n = 7
+        q = rng.standard_normal((n, 5))
+        k = rng.standard_normal((n, 5))
+        v = rng.standard_normal((n, 3))
+        o, lse = att.head_forward(q, k, v, 0.6, causal)
+        assert o.shape == (n, 3)
+        o2, lse2 = SC.forward(q.tolist(), k.tolist(), v.tolist(), 0.6, causal)
+        np.testing.assert_allclose(o, o2, rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(lse, lse2, rtol=1e-13, atol=1e-13)
+    o, _ = att.head_forward(q, k, v, 0.0, False)
+    np.testing.assert_allclose(o, np.broadcast_to(v.mean(axis=0), o.shape), atol=1e-14)
+
+
+def test_asymmetric_head_dims():
+    check_asymmetric_head_dims(A)
+
+
 def test_fully_masked_row():
     # a query that sees no key: O = 0, LSE = -inf, no gradient
     q = np.ones((1, 2)); k = np.ones((3, 2)); v = np.ones((3, 2))
