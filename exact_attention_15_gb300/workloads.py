@@ -11,7 +11,8 @@ sequence workload, the sequence lengths of the packed workload) come from a
 second generator seeded with ``seed + 7``.
 
 Shapes follow the FlashAttention-4 benchmark setup (papercache.org summary,
-"experimental setup": 32k tokens, hidden 2048, head dims 64/128, causal and not)
+"experimental setup": 32k tokens, hidden 2048, head dims 64/128 and the (192, 128)
+query-key / value head dimensions of DeepSeek V3 with 16 heads, causal and not)
 and the FlashAttention-1 kernel analysis shape (wq-win.github.io, section 4:
 sequence 1024, head dim 64, 16 heads, batch 64).
 """
