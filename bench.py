@@ -45,6 +45,8 @@ def parse():
                     help="override the batch size (small cases for profiling)")
     ap.add_argument("--causal", action="store_true", help="causal variant of the workload")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--bwd-variant", default="one_cta", choices=["one_cta", "pair"],
+                    help="backward main kernel at d = 128 (the CTA-pair kernel is kept for measurement)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -225,6 +227,8 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     binding.load()
+    if args.bwd_variant == "pair":
+        binding.attn_set_bwd_variant(binding.BWD_CTA_PAIR)
 
     name = args.workload
     if args.causal and not name.endswith("_causal") and name + "_causal" in W.WORKLOADS:
@@ -438,7 +442,7 @@ def main():
             "config": {"workload": f"{w.name}: " + (w.note or f"B{B} H{H} N{N} d{d}") +
                                    (", fwd only" if fwd_only else ", fwd+bwd"),
                        "global_batch": B * world, "seq_len": N, "heads": H, "kv_heads": H_kv,
-                       "head_dim": d, "head_dim_v": d_v,
+                       "head_dim": d, "head_dim_v": d_v, "bwd_variant": args.bwd_variant,
                        "parallelism": f"replicas x{world}",
                        "l2": f"inputs larger than L2 (q, k, v, o, dO: {q.numel() * 2 / 2**20:.0f} MiB each)"
                              if q.numel() * 2 * 5 > 129e6 else "inputs smaller than L2 (L2 not flushed)"},

@@ -40,6 +40,7 @@ _SIGS = {
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_debug_exp2": (_I, [_P, _P, _I, _I, _P]),
     "attn_set_wait_limit": (ctypes.c_longlong, [ctypes.c_longlong]),
+    "attn_set_bwd_variant": (_I, [_I]),
     "attn_debug_inject": (_I, [_I]),
     "attn_debug_stall": (_I, [_P]),
     "attn_profile_enable": (_I, [_I]),
@@ -51,6 +52,8 @@ KERNEL_NAMES = {1: "attn_fwd_kernel", 2: "attn_bwd_pre_kernel", 3: "attn_bwd_mai
                 7: "fwd_plan_kernel"}
 FAULT_NONE = 0
 FAULT_SKIP_DQ_RELEASE = 1
+BWD_ONE_CTA = 0
+BWD_CTA_PAIR = 1
 
 
 class ProfileRecord(ctypes.Structure):
@@ -148,6 +151,12 @@ def attn_debug_stall(stream=None) -> int:
 
 def attn_set_wait_limit(cycles: int) -> int:
     return load().attn_set_wait_limit(int(cycles))
+
+
+def attn_set_bwd_variant(variant: int) -> int:
+    """BWD_ONE_CTA (default) or BWD_CTA_PAIR for the d = 128 backward; returns
+    the previous selection (-1 for an unknown value)."""
+    return load().attn_set_bwd_variant(int(variant))
 
 
 def attn_profile_enable(enable: bool) -> int:

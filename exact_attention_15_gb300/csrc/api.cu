@@ -41,6 +41,7 @@ int* g_err_ptr[kMaxDevices] = {};
 int g_dev_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 unsupported
 long long g_wait_limit = 2000000000ll;  // about one second of SM clock
 int g_fault = 0;                        // host-injected fault, see attn_debug_inject
+int g_bwd_variant = ATTN_BWD_ONE_CTA;   // backward main kernel at d = 128
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int current_device(int* dev) {
@@ -170,11 +171,11 @@ int l2_section_heads(int H_q, int H_kv, long long rows, int width) {
   return static_cast<int>(kv_per_sec) * (H_q / H_kv);
 }
 
-// 4-D map over a [batch, rows, heads, d] bf16 tensor, one box = 128 rows x 64
-// columns of one head, 128-byte swizzle (so the tile lands in shared memory in
+// 4-D map over a [batch, rows, heads, d] bf16 tensor, one box = 128 (or
+// box_rows) rows x 64 columns of one head, 128-byte swizzle (so the tile lands in shared memory in
 // the layout the tcgen05 descriptors expect).
 int encode_rows_map(CUtensorMap* m, const void* base, int d, int heads, long long rows,
-                    long long batch, bool fp32 = false) {
+                    long long batch, bool fp32 = false, unsigned box_rows = 128) {
   const cuuint64_t es_bytes = fp32 ? 4 : 2;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
                         static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(batch)};
@@ -182,7 +183,7 @@ int encode_rows_map(CUtensorMap* m, const void* base, int d, int heads, long lon
                            static_cast<cuuint64_t>(d) * es_bytes * heads,
                            static_cast<cuuint64_t>(d) * es_bytes * heads * rows};
   // 128 bytes of the innermost dimension per box row: 64 bf16 or 32 fp32
-  cuuint32_t box[4] = {fp32 ? 32u : 64u, 1, 128, 1};
+  cuuint32_t box[4] = {fp32 ? 32u : 64u, 1, box_rows, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = g_encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                         4, const_cast<void*>(base), dims, strides, box, es,
@@ -256,16 +257,25 @@ struct BwdPlan {
   size_t acc_off, dvec_off, sem_off, total;
 };
 
+bool bwd_uses_pairs(int d) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  return d == 128 && g_bwd_variant == ATTN_BWD_CTA_PAIR;
+}
+
+// The workspace size does not depend on `pairs` (only the work count does).
 bool bwd_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d, bool varlen, bool det,
-              BwdPlan* pl) {
+              bool pairs, BwdPlan* pl) {
+  // work items: key tiles of 128 rows, or key pairs of 256 rows (one per CTA
+  // pair)
+  const long long kt = pairs ? 256 : 128;
   if (varlen) {
     pl->rows_q = N_q;
     pl->slots = (static_cast<long long>(N_q) + 127ll * B) / 128;
-    pl->n_work = (static_cast<long long>(N_k) + 127ll * B) / 128 * H_kv;
+    pl->n_work = (static_cast<long long>(N_k) + (kt - 1) * B) / kt * H_kv;
   } else {
     pl->rows_q = static_cast<long long>(B) * N_q;
     pl->slots = static_cast<long long>(B) * ((N_q + 127) / 128);
-    pl->n_work = static_cast<long long>(B) * H_kv * ((N_k + 127) / 128);
+    pl->n_work = static_cast<long long>(B) * H_kv * ((N_k + kt - 1) / kt);
   }
   if (pl->n_work > 0x7fffffffll || pl->slots * H_q > 0x7ffffffell) return false;
   pl->acc_off = 0;
@@ -334,6 +344,14 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103 (GB300 class)";
     default: return "unknown status";
   }
+}
+
+int attn_set_bwd_variant(int variant) {
+  if (variant != ATTN_BWD_ONE_CTA && variant != ATTN_BWD_CTA_PAIR) return -1;
+  std::lock_guard<std::mutex> lock(g_mu);
+  const int old = g_bwd_variant;
+  g_bwd_variant = variant;
+  return old;
 }
 
 long long attn_set_wait_limit(long long cycles) {
@@ -438,7 +456,7 @@ size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int N_q, int N_k, int 
                   &s) != ATTN_OK)
     return 0;
   BwdPlan pl;
-  if (!bwd_plan(B, H_q, H_kv, N_q, N_k, d, varlen != 0, deterministic != 0, &pl)) return 0;
+  if (!bwd_plan(B, H_q, H_kv, N_q, N_k, d, varlen != 0, deterministic != 0, false, &pl)) return 0;
   return pl.total;
 }
 
@@ -458,7 +476,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
       (seqlens && (reinterpret_cast<uintptr_t>(seqlens) & 3u)))
     return ATTN_ERR_ALIGNMENT;
   BwdPlan pl;
-  if (!bwd_plan(B, H_q, H_kv, N_q, N_k, d, seqlens != nullptr, deterministic != 0, &pl))
+  const bool pairs = bwd_uses_pairs(d);
+  if (!bwd_plan(B, H_q, H_kv, N_q, N_k, d, seqlens != nullptr, deterministic != 0, pairs, &pl))
     return ATTN_ERR_BAD_SHAPE;
   if (B == 0) return ATTN_OK;
   const bool empty = (N_q == 0 || N_k == 0);
@@ -480,12 +499,18 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
     return ATTN_OK;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  CUtensorMap maps[5];
+  // q, k, v, dO (128-row boxes), the fp32 dQ accumulator (128-row boxes, 64 on
+  // CTA pairs), and at d = 128 q and dO with 64-row boxes
+  CUtensorMap maps[7];
   if (encode_rows_map(&maps[0], q, d, H_q, s.q_rows, s.q_batch) != ATTN_OK ||
       encode_rows_map(&maps[1], k, d, H_kv, s.k_rows, s.q_batch) != ATTN_OK ||
       encode_rows_map(&maps[2], v, d, H_kv, s.k_rows, s.q_batch) != ATTN_OK ||
       encode_rows_map(&maps[3], dout, d, H_q, s.q_rows, s.q_batch) != ATTN_OK ||
-      encode_rows_map(&maps[4], ws + pl.acc_off, d, H_q, s.q_rows, s.q_batch, true) != ATTN_OK)
+      encode_rows_map(&maps[4], ws + pl.acc_off, d, H_q, s.q_rows, s.q_batch, true,
+                      pairs ? 64u : 128u) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+  if (pairs && (encode_rows_map(&maps[5], q, d, H_q, s.q_rows, s.q_batch, false, 64u) != ATTN_OK ||
+                encode_rows_map(&maps[6], dout, d, H_q, s.q_rows, s.q_batch, false, 64u) != ATTN_OK))
     return ATTN_ERR_CUDA;
 
   BwdParams p;
@@ -505,6 +530,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.err = err;
   p.wait_limit = g_wait_limit;
   p.fault = g_fault;
+  p.pairs = pairs ? 1 : 0;
   const int n_sem = static_cast<int>(pl.slots * H_q);
   if (launch_attn_bwd(p, maps, cs, pl.rows_q, n_sem, static_cast<int>(pl.n_work)) != cudaSuccess)
     return ATTN_ERR_CUDA;

@@ -190,22 +190,7 @@ __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const BwdParams p, l
 
 // ------------------------------------------------------------------ main
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
-}
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 
-// Byte offset inside a 128-byte-swizzled [rows x 64 bf16] block of element
-// (row, col): the 16-byte chunk index is XORed with row % 8.
-__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk16) {
-  return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((chunk16 ^ (row & 7)) << 4));
-}
 
 template <int D>
 __global__ void __launch_bounds__(512, 1)
@@ -655,6 +640,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
 // ------------------------------------------------------------------ host side
 
+cudaError_t launch_attn_bwd_pair_main(const BwdParams& p, const CUtensorMap* maps, int n_pairs,
+                                      int* ticket, cudaStream_t st);
+
 template <int D>
 static cudaError_t launch_bwd_impl(const BwdParams& p, const CUtensorMap* maps, cudaStream_t st,
                                    long long rows_q, int n_sem, int n_work) {
@@ -668,7 +656,12 @@ static cudaError_t launch_bwd_impl(const BwdParams& p, const CUtensorMap* maps, 
   cudaError_t e = cudaGetLastError();
   prof_end(slot, st);
   if (e != cudaSuccess) return e;
-  if (n_work > 0) {
+  if (n_work > 0 && D == 128 && p.pairs) {
+    // CTA pairs: n_work pairs of 256 keys
+    int* ticket = p.deterministic ? p.sem + n_sem : nullptr;
+    e = launch_attn_bwd_pair_main(p, maps, n_work, ticket, st);
+    if (e != cudaSuccess) return e;
+  } else if (n_work > 0) {
     using Cfg = BwdCfg<D>;
     auto kern = attn_bwd_main_kernel<D>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);

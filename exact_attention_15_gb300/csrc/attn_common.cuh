@@ -57,6 +57,7 @@ struct BwdParams {
   int* err;
   long long wait_limit;
   int fault;            // host-injected fault for failure tests (0 = none)
+  int pairs;            // d = 128: run the CTA-pair main kernel
 };
 
 // Kernel tracing (host side, implemented next to the C ABI). prof_begin
@@ -65,6 +66,22 @@ enum KernelId : int { kKFwd = 1, kKBwdPre = 2, kKBwdMain = 3, kKBwdPost = 4, kKE
                       kKStall = 6, kKFwdPlan = 7 };
 int prof_begin(int kernel, cudaStream_t stream);
 void prof_end(int slot, cudaStream_t stream);
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Byte offset inside a 128-byte-swizzled [rows x 64 bf16] block of element
+// (row, col): the 16-byte chunk index is XORed with row % 8.
+__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk16) {
+  return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((chunk16 ^ (row & 7)) << 4));
+}
 
 // Records the first device-side failure; never traps.
 __device__ __forceinline__ void record_error(int* err, int code) {

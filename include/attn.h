@@ -212,6 +212,21 @@ int attn_debug_inject(int fault);
 int attn_debug_stall(attn_stream_t stream);
 
 /*
+ * Selects the backward main kernel used at d = 128 by later attn_bwd calls in
+ * this process: ATTN_BWD_ONE_CTA (default) runs one CTA per 128-key tile;
+ * ATTN_BWD_CTA_PAIR runs the 2-CTA backward of the FlashAttention-4 summary,
+ * section 3.2.3 (clusters of two CTAs per 256 keys, M = 256 tcgen05 MMAs with
+ * operand B split between the CTAs, half of dS exchanged through distributed
+ * shared memory, each CTA reducing 64 rows of every dQ tile). Both give results
+ * within the same tolerances; on GB300 the pair kernel is the slower one, so it
+ * is kept for measurement. d = 64 always uses the one-CTA kernel. Returns the
+ * previous selection, or -1 (and changes nothing) for an unknown value.
+ */
+#define ATTN_BWD_ONE_CTA 0
+#define ATTN_BWD_CTA_PAIR 1
+int attn_set_bwd_variant(int variant);
+
+/*
  * Sets the cycle budget of every bounded device-side wait for later launches
  * on this process (default about one second of SM clock). Returns the old value.
  */
