@@ -36,7 +36,7 @@ WORKLOAD = "mid"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD,
@@ -84,7 +84,8 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """Samples nvidia-smi every 200 ms while the timed region runs."""
+    """Samples nvidia-smi every 50 ms; only the samples after mark() (taken
+    while the timed region runs) are summarised."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -99,7 +100,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -109,6 +110,9 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+
+    def mark(self):
+        self.first = len(self.lines)
 
     def stop(self):
         if self.proc is None:
@@ -120,7 +124,7 @@ class ClockSampler:
             self.proc.kill()
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in self.lines[getattr(self, "first", 0):]:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -155,6 +159,21 @@ def traffic_for(kernel, workload):
     return rec.get("dram_bytes_per_launch")
 
 
+# ------------------------------------------------------------------ shared description of the step
+
+def step_metric(fwd_only):
+    return ("attention fwd TFLOP/s (bf16, 1xGB300)" if fwd_only
+            else "attention fwd+bwd TFLOP/s (bf16, 1xGB300)")
+
+
+def step_config(w, B, N, H, H_kv, d, d_v, fwd_only, world, bwd_variant, l2_note):
+    return {"workload": f"{w.name}: " + (w.note or f"B{B} H{H} N{N} d{d}") +
+                        (", fwd only" if fwd_only else ", fwd+bwd"),
+            "global_batch": B * world, "seq_len": N, "heads": H, "kv_heads": H_kv,
+            "head_dim": d, "head_dim_v": d_v, "bwd_variant": bwd_variant,
+            "parallelism": f"replicas x{world}", "l2": l2_note}
+
+
 # ------------------------------------------------------------------ reference arm (oracle)
 
 def run_reference(args, rank, world):
@@ -180,34 +199,50 @@ def run_reference(args, rank, world):
     sec = sum(times) / len(times)
     value = flops / sec / 1e12
     cores = os.cpu_count()
+    config = step_config(w, w.B, w.N, w.H_q, w.H_kv, w.d, w.d, False, world, args.bwd_variant,
+                         "host memory (oracle)")
+    config["step_sample"] = "1 (batch, head) pair of the workload per step, all query rows"
     line = {
-        "impl": "reference", "metric": "attention fwd+bwd TFLOP/s (bf16 inputs)", "value": value,
+        "impl": "reference", "metric": step_metric(False), "value": value,
         "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: B4 H16 N8192 d128 non-causal", "step_sample": "1 (batch, head) pair"},
+        "config": config,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": "one (batch, head) pair of the workload, all 8192 query rows, fwd+bwd, numpy fp64 BLAS"},
+                         "sample": f"one (batch, head) pair of the workload per step ({w.N} query rows, "
+                                   f"d={w.d}), fwd+bwd, numpy fp64 BLAS on all host cores"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline_sample():
-    """The oracle on a bounded sample (one (b, h) pair), timed on the host."""
+def cpu_baseline_sample(min_seconds=10.0, max_pairs=32):
+    """The oracle as it stands on a bounded sample: whole (batch, head) pairs of
+    the workload, fwd + bwd, until at least `min_seconds` of host time."""
     import oracle
     from exact_attention_15_gb300 import workloads as W
     w = W.WORKLOADS[WORKLOAD]
-    inp = W.custom(1, 1, 1, w.N, w.N, w.d, w.scale, w.causal, seed=w.seed)
+    inp = W.custom(w.B, w.H_q, w.H_kv, w.N, w.N, w.d, w.scale, w.causal, seed=w.seed)
     f64 = W.bf16_bits_to_f64
-    q, k, v, do = (f64(x[0, :, 0, :]) for x in (inp.q, inp.k, inp.v, inp.do))
-    oracle.head_backward(q[:512], k, v, do[:512], w.scale, w.causal)  # warm BLAS
+    pairs = [(b, h) for b in range(w.B) for h in range(w.H_q)]
+    q0 = f64(inp.q[0, :512, 0, :])
+    oracle.head_backward(q0, f64(inp.k[0, :, 0, :]), f64(inp.v[0, :, 0, :]), f64(inp.do[0, :512, 0, :]),
+                         w.scale, w.causal)  # warm BLAS
+    g = w.H_q // w.H_kv
     t0 = time.perf_counter()
-    oracle.head_backward(q, k, v, do, w.scale, w.causal)
+    n = 0
+    for b, h in pairs[:max_pairs]:
+        q, k, v, do = (f64(inp.q[b, :, h, :]), f64(inp.k[b, :, h // g, :]), f64(inp.v[b, :, h // g, :]),
+                       f64(inp.do[b, :, h, :]))
+        oracle.head_backward(q, k, v, do, w.scale, w.causal)
+        n += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
     sec = time.perf_counter() - t0
-    flops = W.fwd_flops(1, 1, w.N, w.N, w.d, w.causal) * 3.5
+    flops = W.fwd_flops(1, 1, w.N, w.N, w.d, w.causal) * 3.5 * n
     return {"value": flops / sec / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"one (batch, head) pair of the workload (8192x8192, d=128), fwd+bwd in {sec:.2f} s, numpy fp64 BLAS on all host cores"}
+            "sample": f"{n} (batch, head) pairs of the workload ({w.N}x{w.N}, d={w.d}), fwd+bwd in "
+                      f"{sec:.1f} s, numpy fp64 BLAS on all host cores"}
 
 
 # ------------------------------------------------------------------ our arm
@@ -293,6 +328,7 @@ def main():
     binding.attn_profile_read()
     sampler.start()
     time.sleep(0.3)
+    sampler.mark()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(args.steps):
@@ -434,18 +470,13 @@ def main():
         cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline_sample()
         fwd_ms = kt.get("attn_fwd_kernel", {}).get("avg_ms")
         line = {
-            "metric": ("attention fwd TFLOP/s (bf16, 1xGB300)" if fwd_only
-                       else "attention fwd+bwd TFLOP/s (bf16, 1xGB300)"), "value": value, "unit": "TFLOP/s",
+            "metric": step_metric(fwd_only), "value": value, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": f"{w.name}: " + (w.note or f"B{B} H{H} N{N} d{d}") +
-                                   (", fwd only" if fwd_only else ", fwd+bwd"),
-                       "global_batch": B * world, "seq_len": N, "heads": H, "kv_heads": H_kv,
-                       "head_dim": d, "head_dim_v": d_v, "bwd_variant": args.bwd_variant,
-                       "parallelism": f"replicas x{world}",
-                       "l2": f"inputs larger than L2 (q, k, v, o, dO: {q.numel() * 2 / 2**20:.0f} MiB each)"
-                             if q.numel() * 2 * 5 > 129e6 else "inputs smaller than L2 (L2 not flushed)"},
+            "config": step_config(w, B, N, H, H_kv, d, d_v, fwd_only, world, args.bwd_variant,
+                                  f"inputs larger than L2 (q, k, v, o, dO: {q.numel() * 2 / 2**20:.0f} MiB each)"
+                                  if q.numel() * 2 * 5 > 129e6 else "inputs smaller than L2 (L2 not flushed)"),
             "fwd_tflops": (fwd_flops / (fwd_ms * 1e-3) / 1e12) if fwd_ms else None,
             "kernels": kt,
             "roofline": roofline,
