@@ -5,6 +5,7 @@
 // C++ API: FlashAttention notes, xwysyy.cn, "code structure").
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -140,9 +141,12 @@ int plan_buffer(int dev, cudaStream_t stream, int seqs, PlanBuf* out) {
   return ATTN_OK;
 }
 
-// Grid of the forward. A persistent grid (one CTA per SM, static striding over
-// the work list) overlaps consecutive tiles of a CTA, which saves the start-up
-// and drain of a CTA per tile (about 2 us); one CTA per tile instead lets the
+// Grid of the forward when no balanced schedule is used (packed inputs, or a
+// causal shape first seen while its stream is being captured). A persistent
+// grid (one CTA per SM, static striding over the work list) overlaps
+// consecutive tiles of a CTA, which saves the start-up and drain of a CTA per
+// tile (taken as 2 us here; the gap between two CTAs on one SM measures about
+// 4 us on GB300); one CTA per tile instead lets the
 // hardware block scheduler balance unequal tiles greedily. Equal tiles (fixed
 // length, no mask) always go persistent; otherwise persistence wins when the
 // start-up it saves per SM outweighs the imbalance static striding can leave,
@@ -155,6 +159,95 @@ bool fwd_persistent(long long tiles, int n_sm, bool causal, bool varlen, long lo
   const double per_key_tile_us = width <= 128 ? 0.9 : 1.7 * width / 256.0;
   const double longest_us = static_cast<double>((len + 127) / 128) * per_key_tile_us;
   return saved_us >= longest_us;
+}
+
+// Balanced persistent schedule of the forward for fixed-length inputs with
+// unequal work tiles (causal masks): the work list, in its usual order, is
+// dealt out greedily, each tile to the CTA with the least estimated work so
+// far (longest-processing-time list scheduling; the order already runs the
+// longest tiles of each L2 section first). A tile is estimated at the key tiles
+// of its two query tiles plus a fixed cost of about six key tiles for its
+// start and epilogue (measured on GB300). The lists depend only on the shape
+// and the grid, are built on the host once per shape and kept on the device
+// until the process exits, so a captured graph can keep using them.
+int fwd_tile_units(long long v, int n_mblocks, int H_q, int sec_heads, int N_q, int N_k,
+                   bool causal) {
+  const long long per_b = static_cast<long long>(n_mblocks) * H_q;
+  const int local = static_cast<int>(v % per_b);
+  const int nm = n_mblocks;
+  const int sec = local / (nm * sec_heads);
+  const int r = local - sec * nm * sec_heads;
+  const int h0 = sec * sec_heads;
+  const int hs = std::min(sec_heads, H_q - h0);
+  const int mi = r / hs;
+  const int m = causal ? (nm - 1 - mi) : mi;
+  int units = 0;
+  for (int i = 0; i < 2; ++i) {
+    const int r0 = m * 256 + i * 128;
+    if (r0 >= N_q) continue;
+    int kv_end = N_k;
+    if (causal) kv_end = std::min(kv_end, r0 + 128);
+    units += (kv_end + 127) / 128;
+  }
+  return units;
+}
+
+struct FwdSchedule {
+  int dev, B, H_q, N_q, N_k, causal, sec_heads, grid;
+  int* ptr;  // cta_start [grid + 1] then tile_list [tiles]
+};
+std::mutex g_sched_mu;
+std::vector<FwdSchedule> g_sched;
+
+// Device copy of the balanced schedule; nullptr when it cannot be made now
+// (while the stream is being captured, a new one is not built).
+const int* fwd_schedule(int dev, cudaStream_t stream, int B, int H_q, int N_q, int N_k, bool causal,
+                        int sec_heads, int n_mblocks, int grid) {
+  std::lock_guard<std::mutex> lock(g_sched_mu);
+  for (const FwdSchedule& f : g_sched)
+    if (f.dev == dev && f.B == B && f.H_q == H_q && f.N_q == N_q && f.N_k == N_k &&
+        f.causal == static_cast<int>(causal) && f.sec_heads == sec_heads && f.grid == grid)
+      return f.ptr;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+    return nullptr;
+  const long long tiles = static_cast<long long>(B) * n_mblocks * H_q;
+  if (tiles > (1ll << 22)) return nullptr;  // list of at most 16 MB
+  constexpr long long kFixedUnits = 6;
+  std::vector<int> owner(tiles), count(grid, 0);
+  // min-heap of (estimated work, CTA)
+  std::vector<std::pair<long long, int>> heap;
+  heap.reserve(grid);
+  for (int c = 0; c < grid; ++c) heap.emplace_back(0, c);
+  auto later = [](const std::pair<long long, int>& a, const std::pair<long long, int>& b) {
+    return a > b;
+  };
+  for (long long v = 0; v < tiles; ++v) {
+    std::pop_heap(heap.begin(), heap.end(), later);
+    auto& top = heap.back();
+    owner[v] = top.second;
+    ++count[top.second];
+    top.first += kFixedUnits + fwd_tile_units(v, n_mblocks, H_q, sec_heads, N_q, N_k, causal);
+    std::push_heap(heap.begin(), heap.end(), later);
+  }
+  std::vector<int> host(grid + 1 + tiles);
+  host[0] = 0;
+  for (int c = 0; c < grid; ++c) host[c + 1] = host[c] + count[c];
+  std::vector<int> fill(host.begin(), host.begin() + grid);
+  for (long long v = 0; v < tiles; ++v) host[grid + 1 + fill[owner[v]]++] = static_cast<int>(v);
+  // the copy completes before the schedule is shared: launches on other
+  // streams may use it next
+  void* ptr = nullptr;
+  if (cudaMalloc(&ptr, host.size() * sizeof(int)) != cudaSuccess) return nullptr;
+  if (cudaMemcpyAsync(ptr, host.data(), host.size() * sizeof(int), cudaMemcpyHostToDevice,
+                      stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaFree(ptr);
+    return nullptr;
+  }
+  g_sched.push_back(FwdSchedule{dev, B, H_q, N_q, N_k, causal ? 1 : 0, sec_heads, grid,
+                                static_cast<int*>(ptr)});
+  return static_cast<int*>(ptr);
 }
 
 // Query heads per L2 section of the forward work list: as many whole KV-head
@@ -422,6 +515,8 @@ int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* l
   p.wait_limit = g_wait_limit;
   p.seq_order = nullptr;
   p.tile_start = nullptr;
+  p.tile_list = nullptr;
+  p.cta_start = nullptr;
   p.total_tiles = static_cast<int>(tiles);
   p.n_mblocks = (N_q + 255) / 256;
   // the mean sequence length sizes the L2 sections of packed inputs
@@ -439,10 +534,22 @@ int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* l
   const int n_sm = sm_count(dev);
   if (n_sm <= 0) return ATTN_ERR_CUDA;
   long long grid_x = tiles;
-  if (fwd_persistent(tiles, n_sm, causal != 0, seqlens != nullptr,
-                     seqlens ? (N_k + B - 1) / B : N_k, d_qk + d_v) &&
-      grid_x > n_sm)
-    grid_x = n_sm;
+  if (grid_x > n_sm) {
+    if (fwd_persistent(tiles, n_sm, causal != 0, seqlens != nullptr,
+                       seqlens ? (N_k + B - 1) / B : N_k, d_qk + d_v)) {
+      grid_x = n_sm;
+    } else if (!seqlens) {
+      // long tiles of unequal, known size (causal masks): a balanced
+      // persistent schedule
+      const int* sch = fwd_schedule(dev, cs, B, H_q, N_q, N_k, causal != 0, p.sec_heads,
+                                    p.n_mblocks, n_sm);
+      if (sch) {
+        p.cta_start = sch;
+        p.tile_list = sch + n_sm + 1;
+        grid_x = n_sm;
+      }
+    }
+  }
   if (launch_attn_fwd(d_qk, d_v, tq, tk, tv, p, dim3(static_cast<unsigned>(grid_x)), cs) !=
       cudaSuccess)
     return ATTN_ERR_CUDA;

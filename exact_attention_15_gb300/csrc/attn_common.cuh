@@ -35,6 +35,8 @@ struct FwdParams {
   int* err;             // device error word
   long long wait_limit; // cycles
   // Work list of the forward (longest-processing-time-first order).
+  const int* tile_list;   // balanced schedule: work tiles of CTA c are
+  const int* cta_start;   //   tile_list[cta_start[c] .. cta_start[c + 1]) (nullptr: striding)
   const int* seq_order;   // packed: virtual -> actual sequence, longest first
   const int* tile_start;  // packed: first work tile of each virtual sequence, [B + 1]
   int total_tiles;        // fixed length: B * n_mblocks * H_q

@@ -152,9 +152,16 @@ __device__ __forceinline__ void expand_fwd_work(const FwdParams& p, const FwdWor
 
 // The k-th work tile of this CTA; false past the end of the list.
 __device__ __forceinline__ bool next_tile(const FwdParams& p, int k, FwdTile& t) {
-  const int v = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
-  const int total = p.cu_seqlens ? p.tile_start[p.B] : p.total_tiles;
-  if (v >= total) return false;
+  int v;
+  if (p.tile_list) {
+    const int first = __ldg(p.cta_start + blockIdx.x) + k;
+    if (first >= __ldg(p.cta_start + blockIdx.x + 1)) return false;
+    v = __ldg(p.tile_list + first);
+  } else {
+    v = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+    const int total = p.cu_seqlens ? p.tile_start[p.B] : p.total_tiles;
+    if (v >= total) return false;
+  }
   expand_fwd_work(p, locate_fwd_work(p, v), t);
   return true;
 }

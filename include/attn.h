@@ -91,6 +91,14 @@ typedef enum {
  * the process exits; a later call with more sequences than the buffer holds
  * synchronises that stream once and reallocates it). Make the first packed call
  * on a stream outside stream capture.
+ *
+ * Fixed-length causal shapes with long work tiles run on a persistent grid whose
+ * CTAs take their tiles from a balanced list built on the host. The first call
+ * with a new (shape, device) builds it, copies it into a library-owned device
+ * buffer (cudaMalloc; the call synchronises its stream once) and keeps it until
+ * the process exits; later calls reuse it. A first call made while the stream is
+ * being captured builds nothing and runs one CTA per work tile instead (same
+ * results, slower).
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H_q, int H_kv, int N_q, int N_k, int d, int causal,

@@ -161,6 +161,38 @@ def test_asymmetric_head_dims_forward(name):
     _oracle_fwd_check(inp, o, lse, _all_pairs(inp))
 
 
+@pytest.mark.parametrize("B,H,N,d", [(2, 16, 8192, 64), (1, 16, 8192, 128), (1, 16, 4096, 192)])
+def test_balanced_schedule_writes_every_tile(B, H, N, d):
+    """Causal shapes with long, unequal work tiles run on a persistent grid
+    that takes its tiles from a host-built balanced list. Every output row must
+    be written exactly as the per-tile computation gives it: the outputs start
+    as NaN and must end finite everywhere, a second launch (schedule reused from
+    its cache) must be bit-identical, and sampled heads and rows match the
+    oracle."""
+    from exact_attention_15_gb300 import binding
+    import torch
+    d_v = 128 if d == 192 else d
+    inp = W.custom(B, H, H, N, N, d, causal=True, seed=4242 + d, parts=("q", "k", "v"), d_v=d_v)
+    from gpu_common import device_inputs
+    dev = device_inputs(inp)
+    outs = []
+    for _ in range(2):
+        o = torch.full((B, N, H, d_v), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+        binding.forward(dev["q"], dev["k"], dev["v"], scale=inp.scale, causal=True, out=o, lse=lse)
+        torch.cuda.synchronize()
+        assert binding.attn_check(None) == 0
+        assert not torch.isnan(o).any().item(), "an output tile was not written"
+        assert not torch.isnan(lse).any().item(), "an LSE tile was not written"
+        outs.append((o, lse))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    rng = np.random.default_rng(11)
+    pairs = _sample(rng, _all_pairs(inp), 2)
+    # rows from the first, a middle and the last work tile of the sequence
+    rows = np.array([0, 1, 255, 256, N // 2 - 1, N // 2, N - 257, N - 256, N - 2, N - 1])
+    _oracle_fwd_check(inp, outs[0][0], outs[0][1], pairs, rows)
+
+
 def test_forward_on_concurrent_streams():
     """Forward passes issued on two streams at once (each stream has its own work
     counter) give the same bits as the same passes run one after the other, and
