@@ -208,6 +208,10 @@ const int* fwd_schedule(int dev, cudaStream_t stream, int B, int H_q, int N_q, i
     if (f.dev == dev && f.B == B && f.H_q == H_q && f.N_q == N_q && f.N_k == N_k &&
         f.causal == static_cast<int>(causal) && f.sec_heads == sec_heads && f.grid == grid)
       return f.ptr;
+  // at most kMaxSchedules shapes keep a list (they are never freed: a captured
+  // graph may still use one); further shapes run one CTA per tile
+  constexpr size_t kMaxSchedules = 256;
+  if (g_sched.size() >= kMaxSchedules) return nullptr;
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
     return nullptr;

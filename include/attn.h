@@ -97,8 +97,8 @@ typedef enum {
  * with a new (shape, device) builds it, copies it into a library-owned device
  * buffer (cudaMalloc; the call synchronises its stream once) and keeps it until
  * the process exits; later calls reuse it. A first call made while the stream is
- * being captured builds nothing and runs one CTA per work tile instead (same
- * results, slower).
+ * being captured, or after 256 shapes already hold a list, builds nothing and
+ * runs one CTA per work tile instead (same results, slower).
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int B, int H_q, int H_kv, int N_q, int N_k, int d, int causal,
