@@ -39,10 +39,20 @@
  *   aligned (tensor-memory-accelerator copies need it).
  *
  * Ownership and execution. The caller allocates and owns every buffer; the
- * library never frees caller memory and, apart from attn_bwd's caller-provided
- * workspace, uses no device memory of its own except one error word per
- * device. Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t;
- * NULL is the legacy default stream); none synchronises the host.
+ * library never frees caller memory. Apart from attn_bwd's caller-provided
+ * workspace, the library's own device memory is small and kept until the process
+ * exits:
+ *   - one error word per device;
+ *   - the forward's packed-input plan buffer per (device, stream);
+ *   - the forward's balanced tile lists per causal shape (see attn_fwd).
+ * Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream). The only host synchronisations are the first-time
+ * set-ups named at each call.
+ *
+ * CUDA graphs. Every call only enqueues work on `stream`, so it can be captured
+ * into a CUDA graph and replayed, with new contents in the same buffers. Make
+ * these calls outside capture: the first call of the library on a device, and
+ * the first packed forward call on a stream.
  *
  * Errors. Argument errors are detected on the host before anything is launched
  * and return a non-zero attn_status; no exception crosses the ABI. A launch

@@ -194,9 +194,8 @@ def test_balanced_schedule_writes_every_tile(B, H, N, d):
 
 
 def test_forward_on_concurrent_streams():
-    """Forward passes issued on two streams at once (each stream has its own work
-    counter) give the same bits as the same passes run one after the other, and
-    repeated launches on one stream reuse the counter correctly."""
+    """Forward passes issued on two streams at once give the same bits as the
+    same passes run one after the other, launch after launch."""
     import torch
     from exact_attention_15_gb300 import binding
     probs = [W.custom(seed=s, B=2, H_q=8, H_kv=8, N_q=1500, N_k=1500, d=64, causal=c,
@@ -224,6 +223,53 @@ def test_forward_on_concurrent_streams():
             assert torch.equal(o.view(torch.int16), ref[i][0].view(torch.int16))
             assert torch.equal(lse, ref[i][1])
     _oracle_fwd_check(probs[0], ref[0][0], ref[0][1], [(0, 0), (1, 7)])
+
+
+def test_cuda_graph_capture_and_replay():
+    """Forward and deterministic backward captured in a CUDA graph and replayed on
+    new inputs give the same bits as eager calls. The causal shape is new when the
+    first graph is captured, so its balanced forward schedule is not built during
+    capture and that graph runs one CTA per work tile; the second graph is captured
+    after an eager call built the schedule and uses it. Per-tile results do not
+    depend on the schedule, so all three agree bit for bit."""
+    import torch
+    from exact_attention_15_gb300 import binding
+    from gpu_common import device_inputs
+    B, H, N, d = 1, 16, 6144, 128
+    a = W.custom(B, H, H, N, N, d, causal=True, seed=777)
+    b = W.custom(B, H, H, N, N, d, causal=True, seed=778)
+    dev_a, dev_b = device_inputs(a), device_inputs(b)
+    names = ("q", "k", "v", "do")
+    static = {n: dev_a[n].clone() for n in names}
+
+    def step(t):
+        o, lse = binding.forward(t["q"], t["k"], t["v"], scale=a.scale, causal=True)
+        dq, dk, dv = binding.backward(t["q"], t["k"], t["v"], o, lse, t["do"], scale=a.scale,
+                                      causal=True, deterministic=True)
+        return o, lse, dq, dk, dv
+
+    def capture():
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            outs = step(static)
+        return g, outs
+
+    g1, outs1 = capture()                # shape first seen here: no schedule built
+    eager = [step(dev_a), step(dev_b)]   # builds and uses the schedule
+    torch.cuda.synchronize()
+    g2, outs2 = capture()                # uses the cached schedule
+    for src, ref in ((dev_b, eager[1]), (dev_a, eager[0])):
+        for n in names:
+            static[n].copy_(src[n])
+        for g, outs in ((g1, outs1), (g2, outs2)):
+            g.replay()
+            torch.cuda.synchronize()
+            assert binding.attn_check(None) == 0
+            for x, y in zip(outs, ref):
+                assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x,
+                                   y.view(torch.int16) if y.dtype == torch.bfloat16 else y)
+    _oracle_fwd_check(a, eager[0][0], eager[0][1], [(0, 3)], np.array([0, 127, 128, 3000, N - 1]))
 
 
 def device_inputs_fwd(inp):
