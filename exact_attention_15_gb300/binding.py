@@ -43,6 +43,7 @@ _SIGS = {
     "attn_set_bwd_variant": (_I, [_I]),
     "attn_debug_inject": (_I, [_I]),
     "attn_debug_stall": (_I, [_P]),
+    "attn_debug_fwd_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.c_longlong]),
     "attn_profile_enable": (_I, [_I]),
     "attn_profile_read": (_I, [_P, _I]),
 }
@@ -147,6 +148,36 @@ def attn_debug_inject(fault: int) -> int:
 
 def attn_debug_stall(stream=None) -> int:
     return load().attn_debug_stall(stream)
+
+
+FWD_ONE_CTA_PER_TILE = 0
+FWD_STRIDING = 1
+FWD_BALANCED_LIST = 2
+
+
+def attn_debug_fwd_plan(B, H_q, H_kv, N_q, N_k, d_qk, d_v, causal, varlen, n_sm, want_lists=True):
+    """The forward's launch plan for a shape, computed on the host (no GPU):
+    dict(mode, grid, tiles, sec_heads, n_mblocks) and, for the balanced-list mode,
+    'start' (per-CTA offsets, grid + 1) and 'tiles_of' (the concatenated lists).
+    Raises on an argument error."""
+    info = (ctypes.c_longlong * 5)()
+    lib = load()
+    st = lib.attn_debug_fwd_plan(B, H_q, H_kv, N_q, N_k, d_qk, d_v, int(causal), int(varlen),
+                                 n_sm, ctypes.cast(info, _P), None, 0)
+    if st != 0:
+        raise ValueError(ATTN_STATUS.get(st, st))
+    out = dict(mode=info[0], grid=info[1], tiles=info[2], sec_heads=info[3], n_mblocks=info[4])
+    if want_lists and out["mode"] == FWD_BALANCED_LIST:
+        cap = out["grid"] + 1 + out["tiles"]
+        buf = (ctypes.c_int * cap)()
+        st = lib.attn_debug_fwd_plan(B, H_q, H_kv, N_q, N_k, d_qk, d_v, int(causal), int(varlen),
+                                     n_sm, ctypes.cast(info, _P), ctypes.cast(buf, _P), cap)
+        if st != 0:
+            raise ValueError(ATTN_STATUS.get(st, st))
+        g = out["grid"]
+        out["start"] = list(buf[:g + 1])
+        out["tiles_of"] = list(buf[g + 1:cap])
+    return out
 
 
 def attn_set_wait_limit(cycles: int) -> int:

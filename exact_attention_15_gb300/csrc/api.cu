@@ -192,6 +192,8 @@ int fwd_tile_units(long long v, int n_mblocks, int H_q, int sec_heads, int N_q, 
   return units;
 }
 
+constexpr long long kMaxListTiles = 1ll << 22;  // list of at most 16 MB
+
 struct FwdSchedule {
   int dev, B, H_q, N_q, N_k, causal, sec_heads, grid;
   int* ptr;  // cta_start [grid + 1] then tile_list [tiles]
@@ -201,22 +203,10 @@ std::vector<FwdSchedule> g_sched;
 
 // Device copy of the balanced schedule; nullptr when it cannot be made now
 // (while the stream is being captured, a new one is not built).
-const int* fwd_schedule(int dev, cudaStream_t stream, int B, int H_q, int N_q, int N_k, bool causal,
-                        int sec_heads, int n_mblocks, int grid) {
-  std::lock_guard<std::mutex> lock(g_sched_mu);
-  for (const FwdSchedule& f : g_sched)
-    if (f.dev == dev && f.B == B && f.H_q == H_q && f.N_q == N_q && f.N_k == N_k &&
-        f.causal == static_cast<int>(causal) && f.sec_heads == sec_heads && f.grid == grid)
-      return f.ptr;
-  // at most kMaxSchedules shapes keep a list (they are never freed: a captured
-  // graph may still use one); further shapes run one CTA per tile
-  constexpr size_t kMaxSchedules = 256;
-  if (g_sched.size() >= kMaxSchedules) return nullptr;
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
-    return nullptr;
+// The balanced lists on the host: cta_start [grid + 1] then tile_list [tiles].
+std::vector<int> fwd_schedule_lists(int B, int H_q, int N_q, int N_k, bool causal, int sec_heads,
+                                    int n_mblocks, int grid) {
   const long long tiles = static_cast<long long>(B) * n_mblocks * H_q;
-  if (tiles > (1ll << 22)) return nullptr;  // list of at most 16 MB
   constexpr long long kFixedUnits = 6;
   std::vector<int> owner(tiles), count(grid, 0);
   // min-heap of (estimated work, CTA)
@@ -239,6 +229,28 @@ const int* fwd_schedule(int dev, cudaStream_t stream, int B, int H_q, int N_q, i
   for (int c = 0; c < grid; ++c) host[c + 1] = host[c] + count[c];
   std::vector<int> fill(host.begin(), host.begin() + grid);
   for (long long v = 0; v < tiles; ++v) host[grid + 1 + fill[owner[v]]++] = static_cast<int>(v);
+  return host;
+}
+
+// Device copy of the balanced schedule; nullptr when it cannot be made now
+// (while the stream is being captured, a new one is not built).
+const int* fwd_schedule(int dev, cudaStream_t stream, int B, int H_q, int N_q, int N_k, bool causal,
+                        int sec_heads, int n_mblocks, int grid) {
+  std::lock_guard<std::mutex> lock(g_sched_mu);
+  for (const FwdSchedule& f : g_sched)
+    if (f.dev == dev && f.B == B && f.H_q == H_q && f.N_q == N_q && f.N_k == N_k &&
+        f.causal == static_cast<int>(causal) && f.sec_heads == sec_heads && f.grid == grid)
+      return f.ptr;
+  // at most kMaxSchedules shapes keep a list (they are never freed: a captured
+  // graph may still use one); further shapes run one CTA per tile
+  constexpr size_t kMaxSchedules = 256;
+  if (g_sched.size() >= kMaxSchedules) return nullptr;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+    return nullptr;
+  if (static_cast<long long>(B) * n_mblocks * H_q > kMaxListTiles) return nullptr;
+  const std::vector<int> host =
+      fwd_schedule_lists(B, H_q, N_q, N_k, causal, sec_heads, n_mblocks, grid);
   // the copy completes before the schedule is shared: launches on other
   // streams may use it next
   void* ptr = nullptr;
@@ -266,6 +278,44 @@ int l2_section_heads(int H_q, int H_kv, long long rows, int width) {
   const long long n_sec = (H_kv + fit - 1) / fit;
   const long long kv_per_sec = (H_kv + n_sec - 1) / n_sec;
   return static_cast<int>(kv_per_sec) * (H_q / H_kv);
+}
+
+// Launch plan of the forward: work tiles, L2 sections, and who takes which
+// tile (kFwdOneCtaPerTile, kFwdStriding, kFwdBalancedList). The balanced list
+// is the intent; a call falls back to one CTA per tile when the list cannot be
+// made at that moment (stream capture of a new shape, or the shape cache full).
+enum { kFwdOneCtaPerTile = 0, kFwdStriding = 1, kFwdBalancedList = 2 };
+struct FwdPlan {
+  long long tiles;  // exact for fixed length, an upper bound when packed
+  int n_mblocks;    // 256-row m-blocks per sequence (fixed length; 0 when packed)
+  int sec_heads;
+  int mode;
+  long long grid;
+};
+FwdPlan fwd_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d_qk, int d_v, bool causal,
+                 bool varlen, int n_sm) {
+  FwdPlan f;
+  // work tiles (2 x 128 query rows of one head): exact for fixed length, an
+  // upper bound on sum over sequences of ceil(L / 256) times H_q when packed
+  f.tiles = varlen ? (static_cast<long long>(N_q) + 255ll * B) / 256 * H_q
+                   : static_cast<long long>(B) * ((N_q + 255) / 256) * H_q;
+  f.n_mblocks = varlen ? 0 : (N_q + 255) / 256;
+  // the mean sequence length sizes the L2 sections of packed inputs
+  f.sec_heads = l2_section_heads(H_q, H_kv, varlen ? (N_k + B - 1) / B : N_k, d_qk + d_v);
+  f.mode = kFwdOneCtaPerTile;
+  f.grid = f.tiles;
+  if (f.tiles > n_sm) {
+    if (fwd_persistent(f.tiles, n_sm, causal, varlen, varlen ? (N_k + B - 1) / B : N_k,
+                       d_qk + d_v)) {
+      f.mode = kFwdStriding;
+      f.grid = n_sm;
+    } else if (!varlen && f.tiles <= kMaxListTiles) {
+      // long tiles of unequal, known size (causal masks)
+      f.mode = kFwdBalancedList;
+      f.grid = n_sm;
+    }
+  }
+  return f;
 }
 
 // 4-D map over a [batch, rows, heads, d] bf16 tensor, one box = 128 (or
@@ -500,11 +550,11 @@ int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* l
     return ATTN_ERR_CUDA;
 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  // work tiles (2 x 128 query rows of one head): exact for fixed length, an
-  // upper bound on sum over sequences of ceil(L / 256) times H_q when packed
-  const long long tiles = seqlens
-                              ? (static_cast<long long>(N_q) + 255ll * B) / 256 * H_q
-                              : static_cast<long long>(B) * ((N_q + 255) / 256) * H_q;
+  const int n_sm = sm_count(dev);
+  if (n_sm <= 0) return ATTN_ERR_CUDA;
+  const FwdPlan plan = fwd_plan(B, H_q, H_kv, N_q, N_k, d_qk, d_v, causal != 0,
+                                seqlens != nullptr, n_sm);
+  const long long tiles = plan.tiles;
   if (tiles > 0x7fffffffll) return ATTN_ERR_BAD_SHAPE;
 
   FwdParams p;
@@ -522,9 +572,8 @@ int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* l
   p.tile_list = nullptr;
   p.cta_start = nullptr;
   p.total_tiles = static_cast<int>(tiles);
-  p.n_mblocks = (N_q + 255) / 256;
-  // the mean sequence length sizes the L2 sections of packed inputs
-  p.sec_heads = l2_section_heads(H_q, H_kv, seqlens ? (N_k + B - 1) / B : N_k, d_qk + d_v);
+  p.n_mblocks = plan.n_mblocks;
+  p.sec_heads = plan.sec_heads;
   if (seqlens) {
     PlanBuf pb;
     if ((st = plan_buffer(dev, cs, B, &pb)) != ATTN_OK) return st;
@@ -535,23 +584,16 @@ int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* l
     p.tile_start = start;
     p.n_mblocks = 0;  // per sequence
   }
-  const int n_sm = sm_count(dev);
-  if (n_sm <= 0) return ATTN_ERR_CUDA;
   long long grid_x = tiles;
-  if (grid_x > n_sm) {
-    if (fwd_persistent(tiles, n_sm, causal != 0, seqlens != nullptr,
-                       seqlens ? (N_k + B - 1) / B : N_k, d_qk + d_v)) {
-      grid_x = n_sm;
-    } else if (!seqlens) {
-      // long tiles of unequal, known size (causal masks): a balanced
-      // persistent schedule
-      const int* sch = fwd_schedule(dev, cs, B, H_q, N_q, N_k, causal != 0, p.sec_heads,
-                                    p.n_mblocks, n_sm);
-      if (sch) {
-        p.cta_start = sch;
-        p.tile_list = sch + n_sm + 1;
-        grid_x = n_sm;
-      }
+  if (plan.mode == kFwdStriding) {
+    grid_x = plan.grid;
+  } else if (plan.mode == kFwdBalancedList) {
+    const int* sch = fwd_schedule(dev, cs, B, H_q, N_q, N_k, causal != 0, p.sec_heads,
+                                  p.n_mblocks, n_sm);
+    if (sch) {
+      p.cta_start = sch;
+      p.tile_list = sch + n_sm + 1;
+      grid_x = plan.grid;
     }
   }
   if (launch_attn_fwd(d_qk, d_v, tq, tk, tv, p, dim3(static_cast<unsigned>(grid_x)), cs) !=
@@ -663,6 +705,31 @@ int attn_check(attn_stream_t stream) {
     if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
       return ATTN_ERR_CUDA;
     return ATTN_ERR_TIMEOUT;
+  }
+  return ATTN_OK;
+}
+
+int attn_debug_fwd_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d_qk, int d_v,
+                        int causal, int varlen, int n_sm, long long* info, int* lists,
+                        long long lists_cap) {
+  if (info == nullptr || n_sm <= 0) return ATTN_ERR_NULL_PTR;
+  if (!((d_qk == 64 && d_v == 64) || (d_qk == 128 && d_v == 128) || (d_qk == 192 && d_v == 128)))
+    return ATTN_ERR_UNSUPPORTED_HEADDIM;
+  Shape s;
+  const int st = check_shape(B, H_q, H_kv, N_q, N_k, d_v, causal,
+                             varlen ? reinterpret_cast<const int*>(16) : nullptr, &s);
+  if (st != ATTN_OK) return st;
+  if (static_cast<long long>(B) * (N_q + N_k) * H_q * d_qk > (1ll << 46)) return ATTN_ERR_BAD_SHAPE;
+  const FwdPlan f = fwd_plan(B, H_q, H_kv, N_q, N_k, d_qk, d_v, causal != 0, varlen != 0, n_sm);
+  info[0] = f.mode;
+  info[1] = f.grid;
+  info[2] = f.tiles;
+  info[3] = f.sec_heads;
+  info[4] = f.n_mblocks;
+  if (f.mode == kFwdBalancedList && lists != nullptr && lists_cap >= f.grid + 1 + f.tiles) {
+    const std::vector<int> h = fwd_schedule_lists(B, H_q, N_q, N_k, causal != 0, f.sec_heads,
+                                                  f.n_mblocks, static_cast<int>(f.grid));
+    std::memcpy(lists, h.data(), h.size() * sizeof(int));
   }
   return ATTN_OK;
 }
