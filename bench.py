@@ -374,9 +374,9 @@ def main():
     # end to end through the public binding with host buffers: every step copies
     # its inputs (q, k, v, dO) from pinned host memory and its results (o, lse,
     # dq, dk, dv) back. Timed two ways: serial (copy in, compute, copy out on one
-    # stream) and pipelined (double-buffered device sets, with the copies on their
-    # own streams, so step s+1's inputs and step s-1's results move while step s
-    # computes).
+    # stream) and pipelined (three device buffer sets, with the copies on their own
+    # streams, so step s+1's inputs and step s-1's results move at the same time,
+    # in both directions, while step s computes).
     e2e = None
     if not args.no_e2e:
         names_in = ("q", "k", "v") if fwd_only else ("q", "k", "v", "do")
@@ -386,9 +386,11 @@ def main():
               for n in names_in]
         sets = [dict(q=q, k=k, v=v, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv)]
         sets[0] = {n: t for n, t in sets[0].items() if t is not None}
-        sets.append({n: torch.empty_like(t) for n, t in sets[0].items()})
+        n_sets = 3
+        for _ in range(n_sets - 1):
+            sets.append({n: torch.empty_like(t) for n, t in sets[0].items()})
         hout = [[torch.empty(sets[0][n].shape, dtype=sets[0][n].dtype).pin_memory() for n in names_out]
-                for _ in range(2)]
+                for _ in range(n_sets)]
         h2d = sum(t.numel() * t.element_size() for t in hq)
         d2h = sum(t.numel() * t.element_size() for t in hout[0])
 
@@ -420,16 +422,16 @@ def main():
             copy_out(sets[0], hout[0])
 
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-        in_ready = [torch.cuda.Event() for _ in range(2)]
-        done = [torch.cuda.Event() for _ in range(2)]
-        freed = [torch.cuda.Event() for _ in range(2)]
+        in_ready = [torch.cuda.Event() for _ in range(n_sets)]
+        done = [torch.cuda.Event() for _ in range(n_sets)]
+        freed = [torch.cuda.Event() for _ in range(n_sets)]
 
         def pipelined(n_steps):
             for i in range(n_steps):
-                b_ = i % 2
+                b_ = i % n_sets
                 with torch.cuda.stream(s_in):
-                    if i >= 2:
-                        s_in.wait_event(freed[b_])  # step i-2's results have left this set
+                    if i >= n_sets:
+                        s_in.wait_event(freed[b_])  # that set's earlier results have left it
                     copy_in(sets[b_])
                     in_ready[b_].record(s_in)
                 stream.wait_event(in_ready[b_])
@@ -444,7 +446,7 @@ def main():
 
         for _ in range(2):
             serial_step()
-        pipelined(2)
+        pipelined(n_sets)
         torch.cuda.synchronize()
         ev0.record(stream)
         for _ in range(args.steps):
@@ -462,7 +464,7 @@ def main():
         e2e = {"value": whole_job_value(step_flops, args.steps, world, ms_pipe), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": ms_pipe / args.steps,
-               "mode": "pipelined: double-buffered device sets, copies on their own streams",
+               "mode": "pipelined: three device buffer sets, copies on their own streams",
                "serial": {"value": whole_job_value(step_flops, args.steps, world, ms_serial),
                           "ms_per_step": ms_serial / args.steps}}
 
