@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--bwd-variant", default="one_cta", choices=["one_cta", "pair"],
                     help="backward main kernel at d = 128 (the CTA-pair kernel is kept for measurement)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="backward with ordered (bit-reproducible) dQ accumulation")
     return ap.parse_args()
 
 
@@ -288,12 +290,13 @@ def main():
     cu_ptr = cu.data_ptr() if varlen else None
     o = torch.empty(q.shape[:-1] + (d_v,), dtype=q.dtype, device="cuda")
     lse = torch.empty((H, N) if varlen else (B, H, N), dtype=torch.float32, device="cuda")
+    det = 1 if args.deterministic else 0
     if fwd_only:
         dq = dk = dv = None
         ws_bytes, ws = 0, None
     else:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        ws_bytes = binding.attn_bwd_workspace_bytes(B, H, H_kv, N, N, d, varlen, 0)
+        ws_bytes = binding.attn_bwd_workspace_bytes(B, H, H_kv, N, N, d, varlen, det)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
@@ -307,7 +310,7 @@ def main():
             return
         st = binding.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                               do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                              B, H, H_kv, N, N, d, w.causal, cu_ptr, w.scale, 0, ws.data_ptr(),
+                              B, H, H_kv, N, N, d, w.causal, cu_ptr, w.scale, det, ws.data_ptr(),
                               ws_bytes, sp)
         assert st == 0, st
 
@@ -404,7 +407,7 @@ def main():
             r = binding.attn_bwd(st_["q"].data_ptr(), st_["k"].data_ptr(), st_["v"].data_ptr(),
                                  st_["o"].data_ptr(), st_["lse"].data_ptr(), st_["do"].data_ptr(),
                                  st_["dq"].data_ptr(), st_["dk"].data_ptr(), st_["dv"].data_ptr(),
-                                 B, H, H_kv, N, N, d, w.causal, cu_ptr, w.scale, 0, ws.data_ptr(),
+                                 B, H, H_kv, N, N, d, w.causal, cu_ptr, w.scale, det, ws.data_ptr(),
                                  ws_bytes, sp_)
             assert r == 0, r
 
@@ -479,6 +482,7 @@ def main():
             "config": step_config(w, B, N, H, H_kv, d, d_v, fwd_only, world, args.bwd_variant,
                                   f"inputs larger than L2 (q, k, v, o, dO: {q.numel() * 2 / 2**20:.0f} MiB each)"
                                   if q.numel() * 2 * 5 > 129e6 else "inputs smaller than L2 (L2 not flushed)"),
+            "deterministic_bwd": bool(det),
             "fwd_tflops": (fwd_flops / (fwd_ms * 1e-3) / 1e12) if fwd_ms else None,
             "kernels": kt,
             "roofline": roofline,

@@ -75,11 +75,12 @@ struct BwdTile {
   int sem_base;       // first query-tile slot of this sequence (packed) or batch
 };
 
+template <bool SPT>
 __device__ __forceinline__ bool decode_bwd_tile(const BwdParams& p, int idx, BwdTile& t) {
   if (p.cu_seqlens == nullptr) {
     const int nk = (p.N_k + kTileN - 1) / kTileN;
     if (nk == 0) return false;
-    t.j = idx % nk;
+    t.j = SPT ? nk - 1 - idx % nk : idx % nk;
     const int rest = idx / nk;
     t.h_kv = rest % p.H_kv;
     t.b = rest / p.H_kv;
@@ -101,7 +102,7 @@ __device__ __forceinline__ bool decode_bwd_tile(const BwdParams& p, int idx, Bwd
     if (s >= p.B) return false;
     const int L = p.cu_seqlens[s + 1] - p.cu_seqlens[s];
     const int nk = (L + kTileN - 1) / kTileN;
-    t.j = idx % nk;
+    t.j = SPT ? nk - 1 - idx % nk : idx % nk;
     t.h_kv = idx / nk;
     t.b = s;
     t.row_base = p.cu_seqlens[s];
@@ -114,6 +115,25 @@ __device__ __forceinline__ bool decode_bwd_tile(const BwdParams& p, int idx, Bwd
   t.i_start = p.causal ? t.j : 0;
   if (t.i_start > t.n_qt) t.i_start = t.n_qt;
   return true;
+}
+
+// Query tile of step k of a key tile's walk (per query head). Deterministic
+// order (FlashAttention-4 summary, section 3.2.4): the additions into one dQ
+// tile follow a fixed order, and a key tile waits for its turn. With p.spt the
+// key tiles start in descending order and the additions into query tile i come
+// in walk-step order: under a causal mask a key tile walks up from its diagonal
+// (shortest-processing-time first: the first addition of every key tile is the
+// first into its query tile); without one, key tile j starts its walk at query
+// tile j (same query and key lengths), so at every step each query tile has
+// exactly one new contributor. A key tile's k-th addition then waits only for
+// additions other key tiles make at their steps before k. Otherwise the walk
+// ascends from i_start and the additions come in ascending key-tile order.
+// (SPT is a template argument so that the other kernels keep their code.)
+template <bool SPT>
+__device__ __forceinline__ int bwd_query_tile(const BwdParams& p, const BwdTile& t, int k) {
+  if (!SPT || p.causal) return t.i_start + k;
+  const int i = t.j + k;
+  return i < t.n_qt ? i : i - t.n_qt;
 }
 
 // ------------------------------------------------------------------ pre / post
@@ -192,7 +212,7 @@ __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const BwdParams p, l
 
 
 
-template <int D>
+template <int D, bool SPT>
 __global__ void __launch_bounds__(512, 1)
 attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -215,7 +235,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     bars->work_idx = (ticket != nullptr) ? atomicAdd(ticket, 1) : static_cast<int>(blockIdx.x);
   __syncthreads();
   BwdTile t;
-  if (!decode_bwd_tile(p, bars->work_idx, t)) return;
+  if (!decode_bwd_tile<SPT>(p, bars->work_idx, t)) return;
   const int n_per_head = t.n_qt - t.i_start;
   const int n_it = n_per_head * p.group;
   const long long lim = p.wait_limit;
@@ -268,7 +288,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         for (int it = 0; it < n_it; ++it) {
           const int stage = it & 1;
           const int h = t.h_kv * p.group + it / n_per_head;
-          const int i = t.i_start + it % n_per_head;
+          const int i = bwd_query_tile<SPT>(p, t, it % n_per_head);
           if (!mbar_wait(smem_addr(&bars->q_empty[stage]), ((it >> 1) & 1) ^ 1, lim)) {
             record_error(p.err, kErrTimeout);
             break;
@@ -431,7 +451,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int stage = it & 1;
-      const int i = t.i_start + it % n_per_head;
+      const int i = bwd_query_tile<SPT>(p, t, it % n_per_head);
       if (!(ok = mbar_wait(smem_addr(&bars->q_full[stage]), (it >> 1) & 1, lim))) break;
       if (!(ok = mbar_wait(smem_addr(&bars->s_full), it & 1, lim))) break;
       tc_fence_after();
@@ -556,7 +576,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int h = t.h_kv * p.group + it / n_per_head;
-      const int i = t.i_start + it % n_per_head;
+      const int i = bwd_query_tile<SPT>(p, t, it % n_per_head);
       if (!(ok = mbar_wait(smem_addr(&bars->dq_full), it & 1, lim))) break;
       tc_fence_after();
       uint32_t v[D];
@@ -569,11 +589,13 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       mbar_arrive(smem_addr(&bars->dq_free));
       int* sem = nullptr;
       if (p.deterministic) {
-        // wait until every key tile before this one has added into query tile i
+        // wait until every key tile ahead of this one in query tile i's order
+        // has added into it
         sem = p.sem + (static_cast<size_t>(t.sem_base) + i) * p.H_q + h;
         if (r == 0) {
           const long long t0 = clock64();
-          while (ld_acquire(sem) != t.j) {
+          const int turn = SPT ? it % n_per_head : t.j;
+          while (ld_acquire(sem) != turn) {
             if (clock64() - t0 > lim) { record_error(p.err, kErrTimeout); break; }
           }
         }
@@ -663,7 +685,7 @@ static cudaError_t launch_bwd_impl(const BwdParams& p, const CUtensorMap* maps, 
     if (e != cudaSuccess) return e;
   } else if (n_work > 0) {
     using Cfg = BwdCfg<D>;
-    auto kern = attn_bwd_main_kernel<D>;
+    auto kern = p.spt ? attn_bwd_main_kernel<D, true> : attn_bwd_main_kernel<D, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     int* ticket = p.deterministic ? p.sem + n_sem : nullptr;

@@ -60,6 +60,8 @@ struct BwdParams {
   long long wait_limit;
   int fault;            // host-injected fault for failure tests (0 = none)
   int pairs;            // d = 128: run the CTA-pair main kernel
+  int spt;              // deterministic one-CTA kernel: key tiles in descending order,
+                        // query tiles walked from the key tile's own, dQ added in step order
 };
 
 // Kernel tracing (host side, implemented next to the C ABI). prof_begin

@@ -338,15 +338,32 @@ def test_workload_backward(name, n_groups):
     _oracle_bwd_check(inp, dq, dk, dv, groups)
 
 
-@pytest.mark.parametrize("name", ["varlen_gqa", "short_causal"])
+DET_CUSTOM = {
+    # non-causal, equal lengths: key tiles walk their query tiles from their own
+    "rotated_gqa": dict(B=2, H_q=4, H_kv=2, N_q=1000, N_k=1000, d=128, causal=False),
+    "rotated_packed": dict(B=0, H_q=2, H_kv=1, N_q=0, N_k=0, d=64, causal=False,
+                           seqlens=[300, 0, 129, 700, 1]),
+    # causal, ragged: shortest-processing-time order from the diagonal
+    "spt_ragged": dict(B=1, H_q=4, H_kv=1, N_q=1100, N_k=1100, d=128, causal=True),
+    # different query and key lengths: ascending key-tile order
+    "ascending_cross": dict(B=2, H_q=2, H_kv=2, N_q=300, N_k=700, d=64, causal=False),
+}
+
+
+@pytest.mark.parametrize("name", ["varlen_gqa", "short_causal", "short"] + list(DET_CUSTOM))
 def test_deterministic_backward(name):
-    """Deterministic mode: three runs bit-identical, and within tolerance."""
+    """Deterministic mode: three runs bit-identical, and within tolerance, in each
+    order the library picks for the dQ additions."""
     import torch
-    inp = W.generate(name)
+    if name in DET_CUSTOM:
+        inp = W.custom(seed=300 + len(name), **DET_CUSTOM[name])
+    else:
+        inp = W.generate(name)
     o, lse, dev = run_forward(inp)
     runs = [run_backward(inp, o, lse, dev, deterministic=True) for _ in range(3)]
     for r in runs[1:]:
         for a, b in zip(runs[0], r):
             assert torch.equal(a.view(torch.int16), b.view(torch.int16)), "not bit-identical"
     rng = np.random.default_rng(13)
-    _oracle_bwd_check(inp, *runs[0], _sample(rng, _all_groups(inp), 1))
+    groups = _all_groups(inp) if name in DET_CUSTOM else _sample(rng, _all_groups(inp), 1)
+    _oracle_bwd_check(inp, *runs[0], groups)
