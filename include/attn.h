@@ -149,7 +149,15 @@ size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int N_q, int N_k, int 
  * attn_bwd_workspace_bytes(...) bytes, 256-byte aligned; its contents on entry
  * do not matter and are undefined on return. With deterministic != 0 the dQ
  * reduction across key tiles runs in a fixed order, so dq, dk and dv are
- * bit-identical across runs with the same inputs on the same device.
+ * bit-identical across runs with the same inputs on the same device. That order
+ * (shortest processing time first) is chosen from the shape:
+ *   - causal: walk up from the diagonal;
+ *   - equal query and key lengths, at most one key tile per SM per (batch, KV
+ *     head): a rotated walk;
+ *   - otherwise: ascending key tiles.
+ * The rotated walk needs all key tiles of a (batch, KV head) resident together.
+ * Kernels on other streams that hold SMs for longer than the wait limit
+ * (attn_set_wait_limit) make such a call end with ATTN_ERR_TIMEOUT recorded.
  * FlashAttention-4 summary, sections 2.1 (gradients), 3.2.2 (pipeline),
  * 3.2.4 (deterministic mode).
  */
