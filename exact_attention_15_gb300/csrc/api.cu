@@ -685,17 +685,18 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.fault = g_fault;
   p.pairs = pairs ? 1 : 0;
   // Deterministic order of the dQ additions: under a causal mask, and without
-  // one when queries and keys have equal lengths and every key tile of a
-  // (batch, KV head) can be resident at once (non-causal key tiles wait on one
-  // another in a cycle), the step order that keeps key tiles from stalling;
-  // otherwise ascending key tiles. Packed sequences share q and k lengths; their
-  // key tiles per sequence are at most those of all rows together.
+  // one when queries and keys have equal lengths and the key tiles of a (batch,
+  // KV head) are few (non-causal key tiles wait on one another in a cycle, so
+  // they must be resident together: at most 32, and at most one per SM), the
+  // step order that keeps key tiles from stalling; otherwise ascending key
+  // tiles. Packed sequences share q and k lengths; their key tiles per sequence
+  // are at most those of all rows together.
   p.spt = 0;
   if (deterministic && !pairs) {
     const int n_sm = sm_count(dev);
     if (n_sm <= 0) return ATTN_ERR_CUDA;
     const long long nk = (static_cast<long long>(N_k) + kTileN - 1) / kTileN;
-    p.spt = (causal || ((seqlens || N_q == N_k) && nk <= n_sm)) ? 1 : 0;
+    p.spt = (causal || ((seqlens || N_q == N_k) && nk <= n_sm && nk <= 32)) ? 1 : 0;
   }
   const int n_sem = static_cast<int>(pl.slots * H_q);
   if (launch_attn_bwd(p, maps, cs, pl.rows_q, n_sem, static_cast<int>(pl.n_work)) != cudaSuccess)

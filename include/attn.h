@@ -152,8 +152,8 @@ size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int N_q, int N_k, int 
  * bit-identical across runs with the same inputs on the same device. That order
  * (shortest processing time first) is chosen from the shape:
  *   - causal: walk up from the diagonal;
- *   - equal query and key lengths, at most one key tile per SM per (batch, KV
- *     head): a rotated walk;
+ *   - equal query and key lengths and at most 32 key tiles per (batch, KV head)
+ *     (and at most one per SM): a rotated walk;
  *   - otherwise: ascending key tiles.
  * The rotated walk needs all key tiles of a (batch, KV head) resident together.
  * Kernels on other streams that hold SMs for longer than the wait limit
