@@ -157,16 +157,17 @@ FWD_BALANCED_LIST = 2
 
 def attn_debug_fwd_plan(B, H_q, H_kv, N_q, N_k, d_qk, d_v, causal, varlen, n_sm, want_lists=True):
     """The forward's launch plan for a shape, computed on the host (no GPU):
-    dict(mode, grid, tiles, sec_heads, n_mblocks) and, for the balanced-list mode,
+    dict(mode, grid, tiles, sec_heads, n_mblocks, pair_heads) and, for the balanced-list mode,
     'start' (per-CTA offsets, grid + 1) and 'tiles_of' (the concatenated lists).
     Raises on an argument error."""
-    info = (ctypes.c_longlong * 5)()
+    info = (ctypes.c_longlong * 6)()
     lib = load()
     st = lib.attn_debug_fwd_plan(B, H_q, H_kv, N_q, N_k, d_qk, d_v, int(causal), int(varlen),
                                  n_sm, ctypes.cast(info, _P), None, 0)
     if st != 0:
         raise ValueError(ATTN_STATUS.get(st, st))
-    out = dict(mode=info[0], grid=info[1], tiles=info[2], sec_heads=info[3], n_mblocks=info[4])
+    out = dict(mode=info[0], grid=info[1], tiles=info[2], sec_heads=info[3], n_mblocks=info[4],
+               pair_heads=info[5])
     if want_lists and out["mode"] == FWD_BALANCED_LIST:
         cap = out["grid"] + 1 + out["tiles"]
         buf = (ctypes.c_int * cap)()

@@ -21,7 +21,7 @@ namespace attn {
 cudaError_t launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const FwdParams& p, dim3 grid,
                             cudaStream_t stream);
-cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int H_q, int* seq_order,
+cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int H_q, int pair_heads, int* seq_order,
                             int* tile_start, cudaStream_t stream);
 cudaError_t launch_exp2_probe(const float* x, float* y, int n, int mode, cudaStream_t stream);
 cudaError_t launch_stall_probe(int* err, long long limit, cudaStream_t stream);
@@ -171,19 +171,21 @@ bool fwd_persistent(long long tiles, int n_sm, bool causal, bool varlen, long lo
 // and the grid, are built on the host once per shape and kept on the device
 // until the process exits, so a captured graph can keep using them.
 int fwd_tile_units(long long v, int n_mblocks, int H_q, int sec_heads, int N_q, int N_k,
-                   bool causal) {
-  const long long per_b = static_cast<long long>(n_mblocks) * H_q;
+                   bool causal, int pair) {
+  const int hu = H_q >> pair;  // heads in units of a work tile's heads
+  const long long per_b = static_cast<long long>(n_mblocks) * hu;
   const int local = static_cast<int>(v % per_b);
   const int nm = n_mblocks;
-  const int sec = local / (nm * sec_heads);
-  const int r = local - sec * nm * sec_heads;
-  const int h0 = sec * sec_heads;
-  const int hs = std::min(sec_heads, H_q - h0);
-  const int mi = r / hs;
+  const int su = sec_heads >> pair;
+  const int sec = local / (nm * su);
+  const int r = local - sec * nm * su;
+  const int u0 = sec * su;
+  const int us = std::min(su, hu - u0);
+  const int mi = r / us;
   const int m = causal ? (nm - 1 - mi) : mi;
   int units = 0;
   for (int i = 0; i < 2; ++i) {
-    const int r0 = m * 256 + i * 128;
+    const int r0 = m * (256 >> pair) + (pair ? 0 : i * 128);
     if (r0 >= N_q) continue;
     int kv_end = N_k;
     if (causal) kv_end = std::min(kv_end, r0 + 128);
@@ -195,7 +197,7 @@ int fwd_tile_units(long long v, int n_mblocks, int H_q, int sec_heads, int N_q, 
 constexpr long long kMaxListTiles = 1ll << 22;  // list of at most 16 MB
 
 struct FwdSchedule {
-  int dev, B, H_q, N_q, N_k, causal, sec_heads, grid;
+  int dev, B, H_q, N_q, N_k, causal, sec_heads, grid, pair;
   int* ptr;  // cta_start [grid + 1] then tile_list [tiles]
 };
 std::mutex g_sched_mu;
@@ -205,8 +207,8 @@ std::vector<FwdSchedule> g_sched;
 // (while the stream is being captured, a new one is not built).
 // The balanced lists on the host: cta_start [grid + 1] then tile_list [tiles].
 std::vector<int> fwd_schedule_lists(int B, int H_q, int N_q, int N_k, bool causal, int sec_heads,
-                                    int n_mblocks, int grid) {
-  const long long tiles = static_cast<long long>(B) * n_mblocks * H_q;
+                                    int n_mblocks, int grid, int pair) {
+  const long long tiles = static_cast<long long>(B) * n_mblocks * (H_q >> pair);
   constexpr long long kFixedUnits = 6;
   std::vector<int> owner(tiles), count(grid, 0);
   // min-heap of (estimated work, CTA)
@@ -221,7 +223,8 @@ std::vector<int> fwd_schedule_lists(int B, int H_q, int N_q, int N_k, bool causa
     auto& top = heap.back();
     owner[v] = top.second;
     ++count[top.second];
-    top.first += kFixedUnits + fwd_tile_units(v, n_mblocks, H_q, sec_heads, N_q, N_k, causal);
+    top.first +=
+        kFixedUnits + fwd_tile_units(v, n_mblocks, H_q, sec_heads, N_q, N_k, causal, pair);
     std::push_heap(heap.begin(), heap.end(), later);
   }
   std::vector<int> host(grid + 1 + tiles);
@@ -235,11 +238,12 @@ std::vector<int> fwd_schedule_lists(int B, int H_q, int N_q, int N_k, bool causa
 // Device copy of the balanced schedule; nullptr when it cannot be made now
 // (while the stream is being captured, a new one is not built).
 const int* fwd_schedule(int dev, cudaStream_t stream, int B, int H_q, int N_q, int N_k, bool causal,
-                        int sec_heads, int n_mblocks, int grid) {
+                        int sec_heads, int n_mblocks, int grid, int pair) {
   std::lock_guard<std::mutex> lock(g_sched_mu);
   for (const FwdSchedule& f : g_sched)
     if (f.dev == dev && f.B == B && f.H_q == H_q && f.N_q == N_q && f.N_k == N_k &&
-        f.causal == static_cast<int>(causal) && f.sec_heads == sec_heads && f.grid == grid)
+        f.causal == static_cast<int>(causal) && f.sec_heads == sec_heads && f.grid == grid &&
+        f.pair == pair)
       return f.ptr;
   // at most kMaxSchedules shapes keep a list (they are never freed: a captured
   // graph may still use one); further shapes run one CTA per tile
@@ -248,9 +252,9 @@ const int* fwd_schedule(int dev, cudaStream_t stream, int B, int H_q, int N_q, i
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
     return nullptr;
-  if (static_cast<long long>(B) * n_mblocks * H_q > kMaxListTiles) return nullptr;
+  if (static_cast<long long>(B) * n_mblocks * (H_q >> pair) > kMaxListTiles) return nullptr;
   const std::vector<int> host =
-      fwd_schedule_lists(B, H_q, N_q, N_k, causal, sec_heads, n_mblocks, grid);
+      fwd_schedule_lists(B, H_q, N_q, N_k, causal, sec_heads, n_mblocks, grid, pair);
   // the copy completes before the schedule is shared: launches on other
   // streams may use it next
   void* ptr = nullptr;
@@ -261,7 +265,7 @@ const int* fwd_schedule(int dev, cudaStream_t stream, int B, int H_q, int N_q, i
     cudaFree(ptr);
     return nullptr;
   }
-  g_sched.push_back(FwdSchedule{dev, B, H_q, N_q, N_k, causal ? 1 : 0, sec_heads, grid,
+  g_sched.push_back(FwdSchedule{dev, B, H_q, N_q, N_k, causal ? 1 : 0, sec_heads, grid, pair,
                                 static_cast<int*>(ptr)});
   return static_cast<int*>(ptr);
 }
@@ -287,7 +291,8 @@ int l2_section_heads(int H_q, int H_kv, long long rows, int width) {
 enum { kFwdOneCtaPerTile = 0, kFwdStriding = 1, kFwdBalancedList = 2 };
 struct FwdPlan {
   long long tiles;  // exact for fixed length, an upper bound when packed
-  int n_mblocks;    // 256-row m-blocks per sequence (fixed length; 0 when packed)
+  int pair;         // work tiles of two query heads (causal, even GQA group)
+  int n_mblocks;    // m-blocks (256 rows, 128 with pair) per batch entry (0 when packed)
   int sec_heads;
   int mode;
   long long grid;
@@ -295,11 +300,16 @@ struct FwdPlan {
 FwdPlan fwd_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d_qk, int d_v, bool causal,
                  bool varlen, int n_sm) {
   FwdPlan f;
-  // work tiles (2 x 128 query rows of one head): exact for fixed length, an
-  // upper bound on sum over sequences of ceil(L / 256) times H_q when packed
-  f.tiles = varlen ? (static_cast<long long>(N_q) + 255ll * B) / 256 * H_q
-                   : static_cast<long long>(B) * ((N_q + 255) / 256) * H_q;
-  f.n_mblocks = varlen ? 0 : (N_q + 255) / 256;
+  // work tiles: two 128-row query tiles, either 256 rows of one head or, under a
+  // causal mask with an even GQA group, the same 128 rows of two heads of one KV
+  // head. Exact for fixed length; for packed inputs an upper bound on the sum
+  // over sequences of ceil(L / rows) times the head units.
+  f.pair = (causal && (H_q / H_kv) % 2 == 0) ? 1 : 0;
+  const long long mrows = 256 >> f.pair;
+  const long long hu = H_q >> f.pair;
+  f.tiles = varlen ? (static_cast<long long>(N_q) + (mrows - 1) * B) / mrows * hu
+                   : static_cast<long long>(B) * ((N_q + mrows - 1) / mrows) * hu;
+  f.n_mblocks = varlen ? 0 : static_cast<int>((N_q + mrows - 1) / mrows);
   // the mean sequence length sizes the L2 sections of packed inputs
   f.sec_heads = l2_section_heads(H_q, H_kv, varlen ? (N_k + B - 1) / B : N_k, d_qk + d_v);
   f.mode = kFwdOneCtaPerTile;
@@ -573,13 +583,15 @@ int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* l
   p.cta_start = nullptr;
   p.total_tiles = static_cast<int>(tiles);
   p.n_mblocks = plan.n_mblocks;
+  p.pair_heads = plan.pair;
   p.sec_heads = plan.sec_heads;
   if (seqlens) {
     PlanBuf pb;
     if ((st = plan_buffer(dev, cs, B, &pb)) != ATTN_OK) return st;
     int* order = pb.ptr;
     int* start = order + pb.cap;
-    if (launch_fwd_plan(seqlens, B, H_q, order, start, cs) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (launch_fwd_plan(seqlens, B, H_q, p.pair_heads, order, start, cs) != cudaSuccess)
+      return ATTN_ERR_CUDA;
     p.seq_order = order;
     p.tile_start = start;
     p.n_mblocks = 0;  // per sequence
@@ -589,7 +601,7 @@ int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* l
     grid_x = plan.grid;
   } else if (plan.mode == kFwdBalancedList) {
     const int* sch = fwd_schedule(dev, cs, B, H_q, N_q, N_k, causal != 0, p.sec_heads,
-                                  p.n_mblocks, n_sm);
+                                  p.n_mblocks, n_sm, plan.pair);
     if (sch) {
       p.cta_start = sch;
       p.tile_list = sch + n_sm + 1;
@@ -740,9 +752,10 @@ int attn_debug_fwd_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d_qk, in
   info[2] = f.tiles;
   info[3] = f.sec_heads;
   info[4] = f.n_mblocks;
+  info[5] = f.pair;
   if (f.mode == kFwdBalancedList && lists != nullptr && lists_cap >= f.grid + 1 + f.tiles) {
     const std::vector<int> h = fwd_schedule_lists(B, H_q, N_q, N_k, causal != 0, f.sec_heads,
-                                                  f.n_mblocks, static_cast<int>(f.grid));
+                                                  f.n_mblocks, static_cast<int>(f.grid), f.pair);
     std::memcpy(lists, h.data(), h.size() * sizeof(int));
   }
   return ATTN_OK;

@@ -30,7 +30,10 @@ struct FwdParams {
   const int* cu_seqlens;  // nullptr for fixed length
   int B, H_q, H_kv, N_q, N_k, group;
   int causal;
-  int n_mblocks;        // work tiles (2 x 128 query rows) per (batch, head); fixed length only
+  int n_mblocks;        // m-blocks per batch entry (fixed length only): 256 query rows, or
+                        // 128 with pair_heads
+  int pair_heads;       // 1: a work tile is the same 128 query rows of two adjacent query
+                        // heads of one KV head (causal, even GQA group); 0: 256 rows of one head
   float scale_log2;     // scale * log2(e)
   int* err;             // device error word
   long long wait_limit; // cycles
@@ -39,7 +42,7 @@ struct FwdParams {
   const int* cta_start;   //   tile_list[cta_start[c] .. cta_start[c + 1]) (nullptr: striding)
   const int* seq_order;   // packed: virtual -> actual sequence, longest first
   const int* tile_start;  // packed: first work tile of each virtual sequence, [B + 1]
-  int total_tiles;        // fixed length: B * n_mblocks * H_q
+  int total_tiles;        // fixed length: B * n_mblocks * (H_q >> pair_heads)
   int sec_heads;          // query heads per L2 section (a multiple of H_q / H_kv)
 };
 

@@ -104,7 +104,7 @@ struct FwdBars {
 __device__ __forceinline__ FwdWork locate_fwd_work(const FwdParams& p, int v) {
   FwdWork w;
   if (p.cu_seqlens == nullptr) {
-    const int per_b = p.n_mblocks * p.H_q;
+    const int per_b = p.n_mblocks * (p.H_q >> p.pair_heads);
     w.b = v / per_b;
     w.local = v - w.b * per_b;
     w.row_base = 0;
@@ -125,24 +125,39 @@ __device__ __forceinline__ FwdWork locate_fwd_work(const FwdParams& p, int v) {
   return w;
 }
 
+// Query tile i of a work tile: rows q0 + 128 i of head h, or, with pair_heads,
+// rows q0 of head h + i. Under a causal mask the head pairs give both query
+// tiles the same key tiles, so neither softmax warpgroup waits out the other's
+// extra diagonal tile at the end of a work tile.
+__device__ __forceinline__ int qtile_row(const FwdParams& p, const FwdTile& t, int i) {
+  return t.q0 + (p.pair_heads ? 0 : i * kTileM);
+}
+__device__ __forceinline__ int qtile_head(const FwdParams& p, const FwdTile& t, int i) {
+  return t.h + (p.pair_heads ? i : 0);
+}
+
 __device__ __forceinline__ void expand_fwd_work(const FwdParams& p, const FwdWork& w, FwdTile& t) {
   t.b = w.b;
   t.row_base = w.row_base;
   t.batch_coord = p.cu_seqlens ? 0 : w.b;
   t.Lq = w.L;
   t.Lk = p.cu_seqlens ? w.L : p.N_k;
-  const int nm = (w.L + 2 * kTileM - 1) / (2 * kTileM);
-  const int sec = w.local / (nm * p.sec_heads);
-  const int r = w.local - sec * nm * p.sec_heads;
-  const int h0 = sec * p.sec_heads;
-  const int hs = min(p.sec_heads, p.H_q - h0);
-  const int mi = r / hs;
-  t.h = h0 + (r - mi * hs);
+  // heads in units of the heads of one work tile (1, or 2 with pair_heads)
+  const int pr = p.pair_heads;
+  const int mrows = (2 * kTileM) >> pr;
+  const int nm = (w.L + mrows - 1) / mrows;
+  const int su = p.sec_heads >> pr;
+  const int sec = w.local / (nm * su);
+  const int r = w.local - sec * nm * su;
+  const int u0 = sec * su;
+  const int us = min(su, (p.H_q >> pr) - u0);
+  const int mi = r / us;
+  t.h = (u0 + (r - mi * us)) << pr;
   t.h_kv = t.h / p.group;
   const int m = p.causal ? (nm - 1 - mi) : mi;
-  t.q0 = m * 2 * kTileM;
+  t.q0 = m * mrows;
   for (int i = 0; i < 2; ++i) {
-    const int r0 = t.q0 + i * kTileM;
+    const int r0 = qtile_row(p, t, i);
     t.valid[i] = r0 < t.Lq;
     int kv_end = t.Lk;
     if (p.causal) kv_end = min(kv_end, r0 + kTileM);
@@ -307,8 +322,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (t.n[i] == 0) continue;
             const uint32_t dst = smem_addr(smem + Cfg::kQOff + i * Cfg::kQTileBytes);
             for (int hf = 0; hf < Cfg::kQBlocks; ++hf)
-              tma_load_4d(dst + hf * 16384, &tm_q, qbar, hf * 64, t.h,
-                          t.row_base + t.q0 + i * kTileM, t.batch_coord);
+              tma_load_4d(dst + hf * 16384, &tm_q, qbar, hf * 64, qtile_head(p, t, i),
+                          t.row_base + qtile_row(p, t, i), t.batch_coord);
           }
           for (int it = 0; it < 2 * n_kv; ++it, ++ld) {
             const int j = it >> 1;
@@ -521,7 +536,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (!next_tile(p, k, t)) break;
       const int my_n = i ? t.n[1] : t.n[0];
       const int Lk = t.Lk;
-      const int q0i = t.q0 + i * kTileM;   // first row of this warpgroup's query tile
+      const int q0i = qtile_row(p, t, i);  // first row of this warpgroup's query tile
       const int qrow = q0i + r;            // sequence-relative query row
       float m_used = -INFINITY;
       float l = 0.0f;
@@ -583,9 +598,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const bool row_ok = qrow < t.Lq;
         const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
         const size_t grow = static_cast<size_t>(t.row_base) + qrow;  // packed row
+        const int hq = qtile_head(p, t, i);
         const size_t o_off =
-            p.cu_seqlens ? (grow * p.H_q + t.h) * DV
-                         : ((static_cast<size_t>(t.b) * p.N_q + qrow) * p.H_q + t.h) * DV;
+            p.cu_seqlens ? (grow * p.H_q + hq) * DV
+                         : ((static_cast<size_t>(t.b) * p.N_q + qrow) * p.H_q + hq) * DV;
         uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + o_off);
 #pragma unroll
         for (int cc = 0; cc < DV / 32; ++cc) {
@@ -610,8 +626,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (row_ok) {
           const float lse = (l > 0.0f) ? (m_used * kLn2 + __logf(l)) : -INFINITY;
           const size_t l_off = p.cu_seqlens
-                                   ? static_cast<size_t>(t.h) * p.N_q + grow
-                                   : (static_cast<size_t>(t.b) * p.H_q + t.h) * p.N_q + qrow;
+                                   ? static_cast<size_t>(hq) * p.N_q + grow
+                                   : (static_cast<size_t>(t.b) * p.H_q + hq) * p.N_q + qrow;
           p.lse[l_off] = lse;
         }
       }
@@ -633,8 +649,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // varlen scheduling paragraph). One CTA. Ties keep their input order; with
 // sort == 0 the input order is kept.
 __global__ void __launch_bounds__(1024)
-fwd_plan_kernel(const int* __restrict__ cu_seqlens, int B, int H_q, int sort, int* seq_order,
-                int* tile_start) {
+fwd_plan_kernel(const int* __restrict__ cu_seqlens, int B, int H_q, int pair_heads, int sort,
+                int* seq_order, int* tile_start) {
   extern __shared__ int plan_smem[];
   int* len = plan_smem;        // [B] when sorting
   int* ord = plan_smem + B;    // [B] when sorting
@@ -661,7 +677,8 @@ fwd_plan_kernel(const int* __restrict__ cu_seqlens, int B, int H_q, int sort, in
   auto tiles_of = [&](int vs) {
     const int s = sort ? ord[vs] : vs;
     const int L = sort ? len[s] : (cu_seqlens[s + 1] - cu_seqlens[s]);
-    return (L + 2 * kTileM - 1) / (2 * kTileM) * H_q;
+    const int mrows = (2 * kTileM) >> pair_heads;
+    return (L + mrows - 1) / mrows * (H_q >> pair_heads);
   };
   int local = 0;
   for (int vs = v0; vs < v1; ++vs) local += tiles_of(vs);
@@ -732,7 +749,7 @@ cudaError_t launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUte
 // shared memory); larger batches keep their input order.
 constexpr int kPlanMaxSort = 8192;
 
-cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int H_q, int* seq_order,
+cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int H_q, int pair_heads, int* seq_order,
                             int* tile_start, cudaStream_t stream) {
   const int sort = (B <= kPlanMaxSort) ? 1 : 0;
   const size_t smem = sort ? static_cast<size_t>(2) * B * sizeof(int) : 0;
@@ -740,7 +757,8 @@ cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int H_q, int* seq_orde
                                        2 * kPlanMaxSort * static_cast<int>(sizeof(int)));
   if (e != cudaSuccess) return e;
   const int slot = prof_begin(kKFwdPlan, stream);
-  fwd_plan_kernel<<<1, 1024, smem, stream>>>(cu_seqlens, B, H_q, sort, seq_order, tile_start);
+  fwd_plan_kernel<<<1, 1024, smem, stream>>>(cu_seqlens, B, H_q, pair_heads, sort, seq_order,
+                                              tile_start);
   e = cudaGetLastError();
   prof_end(slot, stream);
   return e;

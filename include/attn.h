@@ -241,21 +241,27 @@ int attn_debug_stall(attn_stream_t stream);
  * Host-only view of the forward's launch plan (FlashAttention-4 summary,
  * section 3.3: work tiles taken longest first), for checking it without a GPU.
  * For the shape of an attn_fwd_dims call (varlen != 0: packed inputs, B
- * sequences of N_q = N_k total rows) on a GPU with n_sm SMs, writes
+ * sequences of N_q = N_k total rows) on a GPU with n_sm SMs, writes six entries
  *   info[0] mode: 0 one CTA per work tile, 1 persistent grid with CTA c taking
  *           tiles c, c + grid, ..., 2 persistent grid over balanced lists
  *   info[1] grid size
- *   info[2] work tiles (two 128-row query tiles of one (batch, head); an upper
- *           bound when packed)
+ *   info[2] work tiles (two 128-row query tiles each; an upper bound when
+ *           packed)
  *   info[3] query heads per L2 section
- *   info[4] 256-row m-blocks per batch entry (0 when packed)
+ *   info[4] m-blocks per batch entry (0 when packed): 256 query rows of one head,
+ *           or 128 rows with info[5]
+ *   info[5] 1 when a work tile holds the same 128 query rows of two adjacent
+ *           query heads of one KV head (causal masks with an even GQA group), so
+ *           both its query tiles visit the same key tiles; 0 for 256 rows of one
+ *           head
  * and, for mode 2 when lists != NULL and lists_cap >= info[1] + 1 + info[2],
  * the lists: lists[0 .. grid] are the CTAs' start offsets into
  * lists[grid + 1 ..], which hold the work-tile indices of CTA c from
  * lists[grid + 1 + lists[c]] to lists[grid + 1 + lists[c + 1] - 1], in the order
  * the CTA takes them. Work tile v is numbered batch outermost, then L2 section,
- * then m-block (longest first), then query head. A real call uses mode 2 only
- * when it can build the list (outside stream capture, at most 256 shapes);
+ * then m-block (longest first), then query head (or head pair). A real call uses
+ * mode 2 only when it can build the list (outside stream capture, at most 256
+ * shapes);
  * otherwise it runs mode 0. Nothing is launched and no device is needed.
  * Returns ATTN_OK, or the argument error attn_fwd_dims would return.
  */

@@ -15,19 +15,24 @@ ONE_CTA, STRIDING, BALANCED = b.FWD_ONE_CTA_PER_TILE, b.FWD_STRIDING, b.FWD_BALA
 FIXED_COST = 6  # the plan's per-tile start-up estimate, in key tiles
 
 
-def work_tile_units(v, B, H_q, N, sec_heads, causal):
+def work_tile_units(v, B, H_q, N, sec_heads, causal, pair=0):
     """Key tiles the two 128-row query tiles of work tile v visit: tiles are
     numbered batch outermost, then sections of sec_heads query heads, then
-    m-blocks (reversed under a causal mask), then the heads of the section."""
-    nm = (N + 255) // 256
-    local = v % (nm * H_q)
-    sec, rest = divmod(local, nm * sec_heads)
-    hs = min(sec_heads, H_q - sec * sec_heads)
+    m-blocks (reversed under a causal mask), then the heads of the section. A
+    work tile is 256 rows of one head, or (pair) the same 128 rows of two
+    heads, so m-blocks are 128 rows and heads count in pairs."""
+    rows = 256 // (1 + pair)
+    heads = H_q // (1 + pair)
+    sec_units = sec_heads // (1 + pair)
+    nm = (N + rows - 1) // rows
+    local = v % (nm * heads)
+    sec, rest = divmod(local, nm * sec_units)
+    hs = min(sec_units, heads - sec * sec_units)
     mi = rest // hs
     m = nm - 1 - mi if causal else mi
     units = 0
     for i in range(2):
-        r0 = 256 * m + 128 * i
+        r0 = rows * m + (0 if pair else 128 * i)
         if r0 >= N:
             continue
         kv_end = min(N, r0 + 128) if causal else N
@@ -72,6 +77,8 @@ def test_argument_errors():
     (1, 16, 16, 4096, 192, 128, 152),   # separate head dimensions
     (3, 12, 4, 6000, 128, 128, 152),    # GQA, ragged length, partial last section
     (2, 8, 8, 5000, 128, 128, 20),      # few SMs
+    (2, 32, 8, 8192, 128, 128, 152),    # even GQA group: head-pair work tiles
+    (1, 16, 4, 3000, 64, 64, 152),      # head pairs, ragged length
 ])
 def test_balanced_lists(B, H_q, H_kv, N, d_qk, d_v, n_sm):
     p = b.attn_debug_fwd_plan(B, H_q, H_kv, N, N, d_qk, d_v, True, False, n_sm)
@@ -79,7 +86,10 @@ def test_balanced_lists(B, H_q, H_kv, N, d_qk, d_v, n_sm):
     tiles, start, lists = p["tiles"], p["start"], p["tiles_of"]
     assert start[0] == 0 and start[-1] == tiles and len(lists) == tiles
     assert sorted(lists) == list(range(tiles)), "every work tile exactly once"
-    cost = {v: FIXED_COST + work_tile_units(v, B, H_q, N, p["sec_heads"], True)
+    pair = p["pair_heads"]
+    assert pair == (1 if (H_q // H_kv) % 2 == 0 else 0)
+    assert tiles == B * ((N + 255 // (1 + pair)) // (256 // (1 + pair))) * (H_q // (1 + pair))
+    cost = {v: FIXED_COST + work_tile_units(v, B, H_q, N, p["sec_heads"], True, pair)
             for v in range(tiles)}
     loads = []
     for c in range(n_sm):
