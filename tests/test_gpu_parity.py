@@ -161,18 +161,22 @@ def test_asymmetric_head_dims_forward(name):
     _oracle_fwd_check(inp, o, lse, _all_pairs(inp))
 
 
-@pytest.mark.parametrize("B,H,N,d", [(2, 16, 8192, 64), (1, 16, 8192, 128), (1, 16, 4096, 192)])
-def test_balanced_schedule_writes_every_tile(B, H, N, d):
+@pytest.mark.parametrize("B,H,N,d,H_kv", [(2, 16, 8192, 64, 16), (1, 16, 8192, 128, 16),
+                                           (1, 16, 4096, 192, 16), (1, 16, 8192, 128, 4),
+                                           (1, 12, 6000, 64, 2)])
+def test_balanced_schedule_writes_every_tile(B, H, N, d, H_kv):
     """Causal shapes with long, unequal work tiles run on a persistent grid
     that takes its tiles from a host-built balanced list. Every output row must
     be written exactly as the per-tile computation gives it: the outputs start
     as NaN and must end finite everywhere, a second launch (schedule reused from
     its cache) must be bit-identical, and sampled heads and rows match the
-    oracle."""
+    oracle. With an even GQA group a work tile holds the same rows of two query
+    heads."""
     from exact_attention_15_gb300 import binding
     import torch
     d_v = 128 if d == 192 else d
-    inp = W.custom(B, H, H, N, N, d, causal=True, seed=4242 + d, parts=("q", "k", "v"), d_v=d_v)
+    inp = W.custom(B, H, H_kv, N, N, d, causal=True, seed=4242 + d + H_kv, parts=("q", "k", "v"),
+                   d_v=d_v)
     from gpu_common import device_inputs
     dev = device_inputs(inp)
     outs = []
