@@ -45,6 +45,8 @@ def parse():
                     help="override the batch size (small cases for profiling)")
     ap.add_argument("--causal", action="store_true", help="causal variant of the workload")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fwd-variant", default="one_cta", choices=["one_cta", "pair"],
+                    help="forward kernel at d = 128 (the CTA-pair kernel is kept for measurement)")
     ap.add_argument("--bwd-variant", default="one_cta", choices=["one_cta", "pair"],
                     help="backward main kernel at d = 128 (the CTA-pair kernel is kept for measurement)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -168,11 +170,11 @@ def step_metric(fwd_only):
             else "attention fwd+bwd TFLOP/s (bf16, 1xGB300)")
 
 
-def step_config(w, B, N, H, H_kv, d, d_v, fwd_only, world, bwd_variant, l2_note):
+def step_config(w, B, N, H, H_kv, d, d_v, fwd_only, world, bwd_variant, l2_note, fwd_variant="one_cta"):
     return {"workload": f"{w.name}: " + (w.note or f"B{B} H{H} N{N} d{d}") +
                         (", fwd only" if fwd_only else ", fwd+bwd"),
             "global_batch": B * world, "seq_len": N, "heads": H, "kv_heads": H_kv,
-            "head_dim": d, "head_dim_v": d_v, "bwd_variant": bwd_variant,
+            "head_dim": d, "head_dim_v": d_v, "fwd_variant": fwd_variant, "bwd_variant": bwd_variant,
             "parallelism": f"replicas x{world}", "l2": l2_note}
 
 
@@ -202,7 +204,7 @@ def run_reference(args, rank, world):
     value = flops / sec / 1e12
     cores = os.cpu_count()
     config = step_config(w, w.B, w.N, w.H_q, w.H_kv, w.d, w.d, False, world, args.bwd_variant,
-                         "host memory (oracle)")
+                         "host memory (oracle)", args.fwd_variant)
     config["step_sample"] = "1 (batch, head) pair of the workload per step, all query rows"
     line = {
         "impl": "reference", "metric": step_metric(False), "value": value,
@@ -266,6 +268,8 @@ def main():
     binding.load()
     if args.bwd_variant == "pair":
         binding.attn_set_bwd_variant(binding.BWD_CTA_PAIR)
+    if args.fwd_variant == "pair":
+        binding.attn_set_fwd_variant(binding.FWD_CTA_PAIR)
 
     name = args.workload
     if args.causal and not name.endswith("_causal") and name + "_causal" in W.WORKLOADS:
@@ -370,9 +374,11 @@ def main():
                 "frac_of_burst": ach / burst, "frac_of_2250": ach / 2250.0}
 
     dominant = max(kt, key=lambda n: kt[n]["total_ms"]) if kt else None
-    flops_of = {"attn_fwd_kernel": fwd_flops, "attn_bwd_main_kernel": 2.5 * fwd_flops}
+    flops_of = {"attn_fwd_kernel": fwd_flops, "attn_fwd_pair_kernel": fwd_flops,
+                "attn_bwd_main_kernel": 2.5 * fwd_flops}
+    fwd_kernel = "attn_fwd_pair_kernel" if args.fwd_variant == "pair" else "attn_fwd_kernel"
     roofline = roof(dominant, flops_of.get(dominant, 0.0)) if dominant in flops_of else None
-    roofline_fwd = roof("attn_fwd_kernel", fwd_flops)
+    roofline_fwd = roof(fwd_kernel, fwd_flops)
 
     # end to end through the public binding with host buffers: every step copies
     # its inputs (q, k, v, dO) from pinned host memory and its results (o, lse,
@@ -495,7 +501,7 @@ def main():
 
     if rank == 0:
         cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline_sample()
-        fwd_ms = kt.get("attn_fwd_kernel", {}).get("avg_ms")
+        fwd_ms = kt.get(fwd_kernel, {}).get("avg_ms")
         line = {
             "metric": step_metric(fwd_only), "value": value, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
@@ -503,7 +509,8 @@ def main():
             "data": "synthetic",
             "config": step_config(w, B, N, H, H_kv, d, d_v, fwd_only, world, args.bwd_variant,
                                   f"inputs larger than L2 (q, k, v, o, dO: {q.numel() * 2 / 2**20:.0f} MiB each)"
-                                  if q.numel() * 2 * 5 > 129e6 else "inputs smaller than L2 (L2 not flushed)"),
+                                  if q.numel() * 2 * 5 > 129e6 else "inputs smaller than L2 (L2 not flushed)",
+                                  fwd_variant=args.fwd_variant),
             "deterministic_bwd": bool(det),
             "fwd_tflops": (fwd_flops / (fwd_ms * 1e-3) / 1e12) if fwd_ms else None,
             "kernels": kt,

@@ -41,6 +41,7 @@ _SIGS = {
     "attn_debug_exp2": (_I, [_P, _P, _I, _I, _P]),
     "attn_set_wait_limit": (ctypes.c_longlong, [ctypes.c_longlong]),
     "attn_set_bwd_variant": (_I, [_I]),
+    "attn_set_fwd_variant": (_I, [_I]),
     "attn_debug_inject": (_I, [_I]),
     "attn_debug_stall": (_I, [_P]),
     "attn_debug_fwd_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.c_longlong]),
@@ -50,11 +51,13 @@ _SIGS = {
 
 KERNEL_NAMES = {1: "attn_fwd_kernel", 2: "attn_bwd_pre_kernel", 3: "attn_bwd_main_kernel",
                 4: "attn_bwd_post_kernel", 5: "exp2_probe_kernel", 6: "stall_probe_kernel",
-                7: "fwd_plan_kernel"}
+                7: "fwd_plan_kernel", 8: "attn_fwd_pair_kernel"}
 FAULT_NONE = 0
 FAULT_SKIP_DQ_RELEASE = 1
 BWD_ONE_CTA = 0
 BWD_CTA_PAIR = 1
+FWD_ONE_CTA = 0
+FWD_CTA_PAIR = 1
 
 
 class ProfileRecord(ctypes.Structure):
@@ -189,6 +192,12 @@ def attn_set_bwd_variant(variant: int) -> int:
     """BWD_ONE_CTA (default) or BWD_CTA_PAIR for the d = 128 backward; returns
     the previous selection (-1 for an unknown value)."""
     return load().attn_set_bwd_variant(int(variant))
+
+
+def attn_set_fwd_variant(variant: int) -> int:
+    """FWD_ONE_CTA (default) or FWD_CTA_PAIR for the d_qk = d_v = 128 forward;
+    returns the previous selection (-1 for an unknown value)."""
+    return load().attn_set_fwd_variant(int(variant))
 
 
 def attn_profile_enable(enable: bool) -> int:

@@ -22,8 +22,9 @@ BUILD = os.path.join(ROOT, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libattn_gb300.so")
 
-SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_pair.cu", "noalloc.cu"]
-HEADERS = ["ptx.cuh", "attn_common.cuh"]
+SOURCES = ["api.cu", "attn_fwd.cu", "attn_fwd_pair.cu", "attn_bwd.cu", "attn_bwd_pair.cu",
+           "noalloc.cu"]
+HEADERS = ["ptx.cuh", "attn_common.cuh", "fwd_softmax.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr"]

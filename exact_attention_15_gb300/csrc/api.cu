@@ -21,6 +21,9 @@ namespace attn {
 cudaError_t launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const FwdParams& p, dim3 grid,
                             cudaStream_t stream);
+cudaError_t launch_attn_fwd_pair(const CUtensorMap& tq, const CUtensorMap& tk_half,
+                                 const CUtensorMap& tv, const FwdParams& p, dim3 grid,
+                                 cudaStream_t stream);
 cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int H_q, int pair_heads, int* seq_order,
                             int* tile_start, cudaStream_t stream);
 cudaError_t launch_exp2_probe(const float* x, float* y, int n, int mode, cudaStream_t stream);
@@ -43,6 +46,7 @@ int g_dev_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 unsupported
 long long g_wait_limit = 2000000000ll;  // about one second of SM clock
 int g_fault = 0;                        // host-injected fault, see attn_debug_inject
 int g_bwd_variant = ATTN_BWD_ONE_CTA;   // backward main kernel at d = 128
+int g_fwd_variant = ATTN_FWD_ONE_CTA;   // forward kernel at d_qk = d_v = 128
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int current_device(int* dev) {
@@ -414,6 +418,43 @@ struct BwdPlan {
   size_t acc_off, dvec_off, sem_off, total;
 };
 
+bool fwd_uses_pairs() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  return g_fwd_variant == ATTN_FWD_CTA_PAIR;
+}
+
+// The d = 128 forward on CTA pairs: one cluster of two CTAs per 512 query rows
+// of one (batch, query head); K is loaded in 64-row halves, one per CTA.
+int fwd_pair(const CUtensorMap& tq, const void* k_base, int k_heads, long long k_rows,
+             const CUtensorMap& tv, long long batch, void* o, float* lse, int B, int H_q,
+             int H_kv, int N_q, int N_k, int causal, const int* seqlens, float scale, int* err,
+             cudaStream_t cs) {
+  CUtensorMap tk_half;
+  if (encode_rows_map(&tk_half, k_base, 128, k_heads, k_rows, batch, false, 64u) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.o = o;
+  p.lse = lse;
+  p.cu_seqlens = seqlens;
+  p.B = B; p.H_q = H_q; p.H_kv = H_kv; p.N_q = N_q; p.N_k = N_k;
+  p.group = H_q / H_kv;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * kLog2e;
+  p.err = err;
+  p.wait_limit = g_wait_limit;
+  constexpr long long kRows = 4 * kTileM;
+  // packed: an upper bound on the sum over sequences of ceil(L / 512); the
+  // pairs past the last block return at once
+  const long long blocks = seqlens ? (static_cast<long long>(N_q) + (kRows - 1) * B) / kRows
+                                   : (static_cast<long long>(N_q) + kRows - 1) / kRows;
+  if (2 * blocks > 0x7fffffffll) return ATTN_ERR_BAD_SHAPE;
+  const dim3 grid(static_cast<unsigned>(2 * blocks), static_cast<unsigned>(H_q),
+                  seqlens ? 1u : static_cast<unsigned>(B));
+  if (launch_attn_fwd_pair(tq, tk_half, tv, p, grid, cs) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
 bool bwd_uses_pairs(int d) {
   std::lock_guard<std::mutex> lock(g_mu);
   return d == 128 && g_bwd_variant == ATTN_BWD_CTA_PAIR;
@@ -511,6 +552,14 @@ int attn_set_bwd_variant(int variant) {
   return old;
 }
 
+int attn_set_fwd_variant(int variant) {
+  if (variant != ATTN_FWD_ONE_CTA && variant != ATTN_FWD_CTA_PAIR) return -1;
+  std::lock_guard<std::mutex> lock(g_mu);
+  const int old = g_fwd_variant;
+  g_fwd_variant = variant;
+  return old;
+}
+
 long long attn_set_wait_limit(long long cycles) {
   std::lock_guard<std::mutex> lock(g_mu);
   const long long old = g_wait_limit;
@@ -560,6 +609,9 @@ int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* l
     return ATTN_ERR_CUDA;
 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (d_qk == 128 && d_v == 128 && fwd_uses_pairs())
+    return fwd_pair(tq, no_keys ? q : k, no_keys ? H_q : H_kv, no_keys ? s.q_rows : s.k_rows, tv,
+                    s.q_batch, o, lse, B, H_q, H_kv, N_q, N_k, causal, seqlens, scale, err, cs);
   const int n_sm = sm_count(dev);
   if (n_sm <= 0) return ATTN_ERR_CUDA;
   const FwdPlan plan = fwd_plan(B, H_q, H_kv, N_q, N_k, d_qk, d_v, causal != 0,

@@ -70,7 +70,7 @@ struct BwdParams {
 // Kernel tracing (host side, implemented next to the C ABI). prof_begin
 // returns a slot (or -1 when tracing is off); prof_end closes it.
 enum KernelId : int { kKFwd = 1, kKBwdPre = 2, kKBwdMain = 3, kKBwdPost = 4, kKExp2 = 5,
-                      kKStall = 6, kKFwdPlan = 7 };
+                      kKStall = 6, kKFwdPlan = 7, kKFwdPair = 8 };
 int prof_begin(int kernel, cudaStream_t stream);
 void prof_end(int slot, cudaStream_t stream);
 

@@ -285,6 +285,23 @@ int attn_debug_fwd_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d_qk, in
 int attn_set_bwd_variant(int variant);
 
 /*
+ * Selects the forward kernel used by later attn_fwd / attn_fwd_dims calls in
+ * this process at d_qk = d_v = 128: ATTN_FWD_ONE_CTA (default) runs two 128-row
+ * query tiles per CTA under the work-list schedule described for attn_fwd;
+ * ATTN_FWD_CTA_PAIR runs the M = 256 forward on CTA pairs (FlashAttention-4
+ * summary, section 2.2, the 2-CTA tensor-core mode): a cluster of two CTAs owns
+ * 512 query rows of one (batch, query head), and one thread issues
+ * cta_group::2 MMAs with the keys of S = Q K^T and the head-dimension columns
+ * of O += P V split between the CTAs. Both give results within the same
+ * tolerances; on GB300 the pair kernel is the slower one, so it is kept for
+ * measurement. Other head dimensions always use the one-CTA kernel. Returns the
+ * previous selection, or -1 (and changes nothing) for an unknown value.
+ */
+#define ATTN_FWD_ONE_CTA 0
+#define ATTN_FWD_CTA_PAIR 1
+int attn_set_fwd_variant(int variant);
+
+/*
  * Sets the cycle budget of every bounded device-side wait for later launches
  * on this process (default about one second of SM clock). Returns the old value.
  */
@@ -298,7 +315,7 @@ long long attn_set_wait_limit(long long cycles);
  * it returns the number of records written, or a negative attn_status.
  * Kernel ids: 1 forward, 2 backward pre (D, zeroing), 3 backward main,
  * 4 backward post (dQ conversion), 5 exp2 test hook, 6 stall test hook, 7 forward
- * planning kernel (packed inputs).
+ * planning kernel (packed inputs), 8 forward on CTA pairs (ATTN_FWD_CTA_PAIR).
  */
 typedef struct {
   int kernel;  /* kernel id, see above */
