@@ -9,8 +9,9 @@ Importing the package does not load the CUDA library; the first call of a
 binding function does, and it fails loudly when the library is missing.
 """
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_status_string",
-           "attn_check", "forward", "backward"]
+__all__ = ["attn_fwd", "attn_fwd_dims", "attn_bwd", "attn_bwd_noalloc", "attn_bwd_workspace_bytes",
+           "attn_status_string", "attn_check", "attn_set_wait_limit", "attn_set_fwd_variant",
+           "attn_set_bwd_variant", "forward", "backward"]
 
 
 def __getattr__(name):

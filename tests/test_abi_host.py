@@ -143,3 +143,43 @@ def test_no_device_is_reported():
     assert _fwd(lib) == 10
     assert _bwd(lib) == 10
     assert _fwd_dims(lib, 192, 128) == 10
+
+
+def test_package_exports_resolve(lib):
+    import exact_attention_15_gb300 as pkg
+    for n in pkg.__all__:
+        assert callable(getattr(pkg, n)), n
+
+
+@pytest.mark.parametrize("which", ["fwd", "bwd"])
+def test_variant_setters(lib, which):
+    """The kernel-variant hooks are host state only: they return the previous
+    selection and reject unknown values without changing it."""
+    from exact_attention_15_gb300 import binding
+    setter = getattr(binding, f"attn_set_{which}_variant")
+    one = getattr(binding, f"{which.upper()}_ONE_CTA")
+    pair = getattr(binding, f"{which.upper()}_CTA_PAIR")
+    old = setter(pair)
+    try:
+        assert setter(pair) == pair
+        assert setter(-3) == -1
+        assert setter(one) == pair
+        assert setter(one) == one
+    finally:
+        setter(old)
+
+
+def test_pair_forward_checks_arguments_first(lib):
+    """With the CTA-pair forward selected, argument errors still come back
+    before anything is launched."""
+    from exact_attention_15_gb300 import binding
+    old = binding.attn_set_fwd_variant(binding.FWD_CTA_PAIR)
+    try:
+        code = {name: c for c, name in binding.ATTN_STATUS.items()}
+        assert _fwd(lib, d=128, H_q=4, H_kv=3) == code["ATTN_ERR_GQA_RATIO"]
+        assert _fwd(lib, d=128, q=A + 8) == code["ATTN_ERR_ALIGNMENT"]
+        assert _fwd(lib, d=128, causal=1, N_k=64) == code["ATTN_ERR_CAUSAL_SHAPE"]
+        assert _fwd(lib, d=96) == code["ATTN_ERR_UNSUPPORTED_HEADDIM"]
+        assert _fwd(lib, d=128, B=0, q=None, k=None, v=None, o=None, lse=None) == 0
+    finally:
+        binding.attn_set_fwd_variant(old)
