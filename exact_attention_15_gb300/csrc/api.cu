@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -43,8 +44,9 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int* g_err_ptr[kMaxDevices] = {};
 int g_dev_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 unsupported
-long long g_wait_limit = 2000000000ll;  // about one second of SM clock
-int g_fault = 0;                        // host-injected fault, see attn_debug_inject
+// read by every launch without the lock, written under it
+std::atomic<long long> g_wait_limit{2000000000ll};  // about one second of SM clock
+std::atomic<int> g_fault{0};                        // host-injected fault, see attn_debug_inject
 int g_bwd_variant = ATTN_BWD_ONE_CTA;   // backward main kernel at d = 128
 int g_fwd_variant = ATTN_FWD_ONE_CTA;   // forward kernel at d_qk = d_v = 128
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -442,7 +444,7 @@ int fwd_pair(const CUtensorMap& tq, const void* k_base, int k_heads, long long k
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * kLog2e;
   p.err = err;
-  p.wait_limit = g_wait_limit;
+  p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
   constexpr long long kRows = 4 * kTileM;
   // packed: an upper bound on the sum over sequences of ceil(L / 512); the
   // pairs past the last block return at once
@@ -562,8 +564,8 @@ int attn_set_fwd_variant(int variant) {
 
 long long attn_set_wait_limit(long long cycles) {
   std::lock_guard<std::mutex> lock(g_mu);
-  const long long old = g_wait_limit;
-  if (cycles > 0) g_wait_limit = cycles;
+  const long long old = g_wait_limit.load();
+  if (cycles > 0) g_wait_limit.store(cycles);
   return old;
 }
 
@@ -628,7 +630,7 @@ int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* l
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * kLog2e;
   p.err = err;
-  p.wait_limit = g_wait_limit;
+  p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
   p.seq_order = nullptr;
   p.tile_start = nullptr;
   p.tile_list = nullptr;
@@ -745,8 +747,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
   p.err = err;
-  p.wait_limit = g_wait_limit;
-  p.fault = g_fault;
+  p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+  p.fault = g_fault.load(std::memory_order_relaxed);
   p.pairs = pairs ? 1 : 0;
   // Deterministic order of the dQ additions: under a causal mask, and without
   // one when queries and keys have equal lengths and the key tiles of a (batch,
@@ -816,7 +818,7 @@ int attn_debug_fwd_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d_qk, in
 int attn_debug_inject(int fault) {
   if (fault != ATTN_FAULT_NONE && fault != ATTN_FAULT_SKIP_DQ_RELEASE) return ATTN_ERR_BAD_SHAPE;
   std::lock_guard<std::mutex> lock(g_mu);
-  g_fault = fault;
+  g_fault.store(fault);
   return ATTN_OK;
 }
 
@@ -826,7 +828,8 @@ int attn_debug_stall(attn_stream_t stream) {
   if (st != ATTN_OK) return st;
   int* err;
   if ((st = device_setup(dev, &err)) != ATTN_OK) return st;
-  return launch_stall_probe(err, g_wait_limit, reinterpret_cast<cudaStream_t>(stream)) ==
+  return launch_stall_probe(err, g_wait_limit.load(std::memory_order_relaxed),
+                            reinterpret_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? ATTN_OK
              : ATTN_ERR_CUDA;
