@@ -180,6 +180,37 @@ def step_config(w, B, N, H, H_kv, d, d_v, fwd_only, world, bwd_variant, l2_note,
 
 # ------------------------------------------------------------------ reference arm (oracle)
 
+def workload_name(args, W):
+    """The named workload both arms run (``--workload``, ``--causal``)."""
+    name = args.workload
+    if args.causal and not name.endswith("_causal") and name + "_causal" in W.WORKLOADS:
+        name += "_causal"
+    return name
+
+
+def oracle_unit_shapes(w, inp=None):
+    """Units of oracle work of a workload: one (batch entry or packed sequence,
+    query head) each, as (query rows, key rows). Packed workloads take their
+    lengths from the generated inputs."""
+    if w.varlen is None:
+        B = w.B if inp is None else inp.B
+        return [(w.N, w.N)] * (B * w.H_q)
+    return [(int(L), int(L)) for L in inp.seqlens() for _ in range(w.H_q)]
+
+
+def oracle_step(oracle, q, k, v, do, w, fwd_only):
+    if fwd_only:
+        oracle.head_forward(q, k, v, w.scale, w.causal)
+    else:
+        oracle.head_backward(q, k, v, do, w.scale, w.causal)
+
+
+def unit_flops(W, w, L_q, L_k, fwd_only):
+    d_v = w.d_v or w.d
+    f = W.fwd_flops(1, 1, L_q, L_k, w.d, w.causal, d_v=d_v)
+    return f if fwd_only else 3.5 * f
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -187,66 +218,98 @@ def run_reference(args, rank, world):
     import oracle
     from exact_attention_15_gb300 import workloads as W
 
-    w = W.WORKLOADS[WORKLOAD]
-    # bounded sample: one (batch, head) pair, every query row, forward + backward
-    inp = W.custom(1, 1, 1, w.N, w.N, w.d, w.scale, w.causal, seed=w.seed)
+    w = W.WORKLOADS[workload_name(args, W)]
+    fwd_only = (w.d_v or w.d) != w.d
+    # bounded sample: one (batch entry or sequence, head) unit per step, every
+    # query row; packed workloads take a unit of the median sequence length
+    if w.varlen is None:
+        L = w.N
+    else:
+        L = int(np.median(W.generate(w.name, parts=("q",)).seqlens()))
+    inp = W.custom(1, 1, 1, L, L, w.d, w.scale, w.causal, seed=w.seed, d_v=w.d_v)
     f64 = W.bf16_bits_to_f64
     q, k, v, do = (f64(x[0, :, 0, :]) for x in (inp.q, inp.k, inp.v, inp.do))
-    flops = W.fwd_flops(1, 1, w.N, w.N, w.d, w.causal) * 3.5
+    flops = unit_flops(W, w, L, L, fwd_only)
     for _ in range(args.warmup):
-        oracle.head_backward(q, k, v, do, w.scale, w.causal)
+        oracle_step(oracle, q, k, v, do, w, fwd_only)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.head_backward(q, k, v, do, w.scale, w.causal)
+        oracle_step(oracle, q, k, v, do, w, fwd_only)
         times.append(time.perf_counter() - t0)
     sec = sum(times) / len(times)
     value = flops / sec / 1e12
     cores = os.cpu_count()
-    config = step_config(w, w.B, w.N, w.H_q, w.H_kv, w.d, w.d, False, world, args.bwd_variant,
-                         "host memory (oracle)", args.fwd_variant)
-    config["step_sample"] = "1 (batch, head) pair of the workload per step, all query rows"
+    config = step_config(w, w.B, w.N, w.H_q, w.H_kv, w.d, w.d_v or w.d, fwd_only, world,
+                         args.bwd_variant, "host memory (oracle)", args.fwd_variant)
+    unit = "(sequence, head) unit of median length" if w.varlen else "(batch, head) pair"
+    config["step_sample"] = f"1 {unit} of the workload per step, all {L} query rows"
+    passes = "fwd" if fwd_only else "fwd+bwd"
     line = {
-        "impl": "reference", "metric": step_metric(False), "value": value,
+        "impl": "reference", "metric": step_metric(fwd_only), "value": value,
         "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"one (batch, head) pair of the workload per step ({w.N} query rows, "
-                                   f"d={w.d}), fwd+bwd, numpy fp64 BLAS on all host cores"},
+                         "sample": f"one {unit} of the workload per step ({L} query rows, "
+                                   f"d={w.d}), {passes}, numpy fp64 BLAS on all host cores"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline_sample(min_seconds=10.0, max_pairs=32):
-    """The oracle as it stands on a bounded sample: whole (batch, head) pairs of
-    the workload, fwd + bwd, until at least `min_seconds` of host time."""
+def cpu_baseline_sample(name, inp, fwd_only, min_seconds=10.0, max_units=32):
+    """The oracle as it stands on a bounded sample of the workload's own inputs:
+    whole (batch entry or sequence, head) units in a seeded order, forward (and
+    backward unless the step is forward only), until at least `min_seconds` of
+    host time; the full-workload time is extrapolated from the measured rate."""
+    import numpy as np
     import oracle
     from exact_attention_15_gb300 import workloads as W
-    w = W.WORKLOADS[WORKLOAD]
-    inp = W.custom(w.B, w.H_q, w.H_kv, w.N, w.N, w.d, w.scale, w.causal, seed=w.seed)
+    w = W.WORKLOADS[name]
     f64 = W.bf16_bits_to_f64
-    pairs = [(b, h) for b in range(w.B) for h in range(w.H_q)]
-    q0 = f64(inp.q[0, :512, 0, :])
-    oracle.head_backward(q0, f64(inp.k[0, :, 0, :]), f64(inp.v[0, :, 0, :]), f64(inp.do[0, :512, 0, :]),
-                         w.scale, w.causal)  # warm BLAS
-    g = w.H_q // w.H_kv
+    g = inp.H_q // inp.H_kv
+    if inp.cu_seqlens is None:
+        units = [(b, h, None) for b in range(inp.B) for h in range(inp.H_q)]
+    else:
+        cu = inp.cu_seqlens
+        units = [(s, h, (int(cu[s]), int(cu[s + 1]))) for s in range(len(cu) - 1)
+                 for h in range(inp.H_q)]
+    order = np.random.default_rng(w.seed).permutation(len(units))
+
+    def slices(u):
+        b, h, span = u
+        if span is None:
+            return (f64(inp.q[b, :, h, :]), f64(inp.k[b, :, h // g, :]), f64(inp.v[b, :, h // g, :]),
+                    f64(inp.do[b, :, h, :]))
+        a, e = span
+        return (f64(inp.q[a:e, h, :]), f64(inp.k[a:e, h // g, :]), f64(inp.v[a:e, h // g, :]),
+                f64(inp.do[a:e, h, :]))
+
+    q0, k0, v0, do0 = slices(units[order[0]])
+    oracle_step(oracle, q0[:512], k0, v0, do0[:512], w, fwd_only)  # warm BLAS
     t0 = time.perf_counter()
-    n = 0
-    for b, h in pairs[:max_pairs]:
-        q, k, v, do = (f64(inp.q[b, :, h, :]), f64(inp.k[b, :, h // g, :]), f64(inp.v[b, :, h // g, :]),
-                       f64(inp.do[b, :, h, :]))
-        oracle.head_backward(q, k, v, do, w.scale, w.causal)
+    n, flops = 0, 0.0
+    for idx in order[:max_units]:
+        q, k, v, do = slices(units[idx])
+        oracle_step(oracle, q, k, v, do, w, fwd_only)
+        flops += unit_flops(W, w, q.shape[0], k.shape[0], fwd_only)
         n += 1
         if time.perf_counter() - t0 >= min_seconds:
             break
     sec = time.perf_counter() - t0
-    flops = W.fwd_flops(1, 1, w.N, w.N, w.d, w.causal) * 3.5 * n
-    return {"value": flops / sec / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{n} (batch, head) pairs of the workload ({w.N}x{w.N}, d={w.d}), fwd+bwd in "
-                      f"{sec:.1f} s, numpy fp64 BLAS on all host cores"}
+    rate = flops / sec
+    total = sum(unit_flops(W, w, a, b, fwd_only) for a, b in oracle_unit_shapes(w, inp))
+    kind = "(sequence, head) units" if inp.cu_seqlens is not None else "(batch, head) pairs"
+    return {"value": rate / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} seeded {kind} of the workload (d={w.d}), "
+                      f"{'fwd' if fwd_only else 'fwd+bwd'} in {sec:.1f} s, numpy fp64 BLAS on all "
+                      f"host cores",
+            "seconds_per_unit": sec / n,
+            "extrapolated_step_s": total / rate,
+            "extrapolated_note": f"extrapolated: the whole workload ({len(units)} units) at the "
+                                 f"measured rate, not measured"}
 
 
 # ------------------------------------------------------------------ our arm
@@ -271,9 +334,7 @@ def main():
     if args.fwd_variant == "pair":
         binding.attn_set_fwd_variant(binding.FWD_CTA_PAIR)
 
-    name = args.workload
-    if args.causal and not name.endswith("_causal") and name + "_causal" in W.WORKLOADS:
-        name += "_causal"
+    name = workload_name(args, W)
     w = W.WORKLOADS[name]
     if args.batch is not None and w.varlen is None:
         inp = W.custom(args.batch, w.H_q, w.H_kv, w.N, w.N, w.d, w.scale, w.causal, seed=w.seed,
@@ -500,7 +561,7 @@ def main():
                           "ms_per_step": ms_serial / args.steps}}
 
     if rank == 0:
-        cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline_sample()
+        cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline_sample(name, inp, fwd_only)
         fwd_ms = kt.get(fwd_kernel, {}).get("avg_ms")
         line = {
             "metric": step_metric(fwd_only), "value": value, "unit": "TFLOP/s",
