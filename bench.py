@@ -414,8 +414,8 @@ def main():
     value = whole_job_value(step_flops, args.steps, world, ms_total)
 
     per_kernel = {}
-    for name, ms in recs:
-        per_kernel.setdefault(name, []).append(ms)
+    for kname, ms in recs:
+        per_kernel.setdefault(kname, []).append(ms)
     kt = {n: {"launches": len(v_), "avg_ms": sum(v_) / len(v_), "total_ms": sum(v_)} for n, v_ in per_kernel.items()}
     tot = sum(x["total_ms"] for x in kt.values()) or 1.0
     for x in kt.values():
@@ -561,7 +561,7 @@ def main():
                           "ms_per_step": ms_serial / args.steps}}
 
     if rank == 0:
-        cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline_sample(name, inp, fwd_only)
+        cpu = None if args.no_cpu_baseline or world > 1 else cpu_baseline_sample(w.name, inp, fwd_only)
         fwd_ms = kt.get(fwd_kernel, {}).get("avg_ms")
         line = {
             "metric": step_metric(fwd_only), "value": value, "unit": "TFLOP/s",
