@@ -167,13 +167,15 @@ def test_brute_force_scalar():
     check_brute_force_scalar(A)
 
 
-def check_finite_differences(att, seed=13):
-    """Central differences of L = sum(O o dO) in float64, h = 1e-6."""
+def check_finite_differences(att, seed=13, d_qk=4, d_v=None):
+    """Central differences of L = sum(O o dO) in float64, h = 1e-6. With d_v the
+    values (and O, dO) have their own width, as in the (192, 128) head
+    dimensions of the FlashAttention-4 benchmark."""
     rng = np.random.default_rng(seed)
     h = 1e-6
     for causal in (False, True):
-        n, d = 6, 4
-        q, k, v, do = _rand_head(rng, n, n, d)
+        n = 6
+        q, k, v, do = _rand_head(rng, n, n, d_qk, d_v)
         scale = 0.8
         r = att.head_backward(q, k, v, do, scale, causal)
 
@@ -196,6 +198,12 @@ def check_finite_differences(att, seed=13):
 
 def test_finite_differences():
     check_finite_differences(A)
+
+
+def test_finite_differences_separate_head_dims():
+    """The backward with query/key width 5 and value width 3: dQ, dK have 5
+    columns, dV 3, all matching central differences."""
+    check_finite_differences(A, seed=31, d_qk=5, d_v=3)
 
 
 # ------------------------------------------------------------------ invariants and closed forms
