@@ -224,6 +224,46 @@ def _shape(q, k, cu_seqlens):
     return B, H_q, k.shape[2], N_q, k.shape[1], d
 
 
+def _check_inputs(q, k, v, cu_seqlens, d_v_equal=False):
+    """Shapes first (so that a mismatch is reported as such), then dtype, device
+    and layout: the C ABI takes sizes from q and k only, so v must match them."""
+    import torch
+    nd = 3 if cu_seqlens is not None else 4
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dim() != nd:
+            raise ValueError(f"{name} must have {nd} dimensions "
+                             f"({'[T, H, d] with cu_seqlens' if nd == 3 else '[B, N, H, d]'}), "
+                             f"got {tuple(t.shape)}")
+    if v.shape[:-1] != k.shape[:-1]:
+        raise ValueError(f"v {tuple(v.shape)} and k {tuple(k.shape)} differ outside the head dimension")
+    if k.shape[-1] != q.shape[-1]:
+        raise ValueError(f"q and k head dimensions differ: {q.shape[-1]} vs {k.shape[-1]}")
+    if nd == 4 and k.shape[0] != q.shape[0]:
+        raise ValueError(f"q and k batch sizes differ: {q.shape[0]} vs {k.shape[0]}")
+    if d_v_equal and v.shape[-1] != q.shape[-1]:
+        raise ValueError("the backward pass needs equal query/key and value head dimensions")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
+    if cu_seqlens is not None:
+        if (cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2
+                or not cu_seqlens.is_contiguous() or cu_seqlens.device != q.device):
+            raise ValueError("cu_seqlens must be a contiguous 1-D int32 tensor of at least two "
+                             "entries on q's device")
+
+
+def _check_tensor(name, t, shape, dtype, device):
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_contiguous() or t.device != device:
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} on "
+                         f"{device}, got {t.dtype} {tuple(t.shape)} on {t.device}")
+
+
+def _lse_shape(B, H_q, N_q, cu_seqlens):
+    return (H_q, N_q) if cu_seqlens is not None else (B, H_q, N_q)
+
+
 def _stream_ptr():
     import torch
     return torch.cuda.current_stream().cuda_stream
@@ -239,16 +279,18 @@ def forward(q, k, v, scale=None, causal=False, cu_seqlens=None, out=None, lse=No
     d_qk and v with d_v columns, bf16 CUDA tensors. Returns (o [.., d_v], lse).
     The default scale is 1/sqrt(d_qk)."""
     import torch
+    _check_inputs(q, k, v, cu_seqlens)
     B, H_q, H_kv, N_q, N_k, d = _shape(q, k, cu_seqlens)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    for t in (q, k, v):
-        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors")
-    o = out if out is not None else torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
-    if lse is None:
-        lse = torch.empty((H_q, N_q) if cu_seqlens is not None else (B, H_q, N_q),
-                          dtype=torch.float32, device=q.device)
+    o_shape = q.shape[:-1] + (v.shape[-1],)
+    if out is not None:
+        _check_tensor("out", out, o_shape, torch.bfloat16, q.device)
+    o = out if out is not None else torch.empty(o_shape, dtype=q.dtype, device=q.device)
+    if lse is not None:
+        _check_tensor("lse", lse, _lse_shape(B, H_q, N_q, cu_seqlens), torch.float32, q.device)
+    else:
+        lse = torch.empty(_lse_shape(B, H_q, N_q, cu_seqlens), dtype=torch.float32, device=q.device)
     cu_ptr = cu_seqlens.data_ptr() if cu_seqlens is not None else None
     d_v = v.shape[-1]
     _check(attn_fwd_dims(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
@@ -261,18 +303,25 @@ def backward(q, k, v, o, lse, dout, scale=None, causal=False, cu_seqlens=None,
              deterministic=False, workspace=None):
     """Returns (dq, dk, dv). The workspace is allocated with torch unless given."""
     import torch
+    _check_inputs(q, k, v, cu_seqlens, d_v_equal=True)
     B, H_q, H_kv, N_q, N_k, d = _shape(q, k, cu_seqlens)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    _check_tensor("o", o, q.shape, torch.bfloat16, q.device)
+    _check_tensor("dout", dout, q.shape, torch.bfloat16, q.device)
+    _check_tensor("lse", lse, _lse_shape(B, H_q, N_q, cu_seqlens), torch.float32, q.device)
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
     nbytes = attn_bwd_workspace_bytes(B, H_q, H_kv, N_q, N_k, d, cu_seqlens is not None, deterministic)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    elif not workspace.is_contiguous() or workspace.device != q.device:
+        raise ValueError("workspace must be a contiguous tensor on q's device")
     cu_ptr = cu_seqlens.data_ptr() if cu_seqlens is not None else None
     _check(attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                     dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                     B, H_q, H_kv, N_q, N_k, d, causal, cu_ptr, scale, deterministic,
-                    workspace.data_ptr(), workspace.numel(), _stream_ptr()), "attn_bwd")
+                    workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr()),
+           "attn_bwd")
     return dq, dk, dv
