@@ -11,9 +11,9 @@
 //                     as its half of B);
 //   O_s += P_s V_j    with the 128 head-dimension columns of V_j split 64 / 64
 //                     (P comes from each CTA's own TMEM).
-// Each instruction does twice the work of a one-CTA instruction and each CTA
-// loads and stores only half of every K and V tile. Softmax, the lazy rescale
-// and the epilogue run per CTA exactly as in the one-CTA kernel.
+// Each instruction does twice the work of a one-CTA instruction, and each CTA
+// loads into its shared memory only half of every K and V tile. Softmax, the
+// lazy rescale and the epilogue run per CTA exactly as in the one-CTA kernel.
 //
 // Synchronisation: the TMA loads of both CTAs and the softmax arrivals of both
 // CTAs are counted on the even CTA's barriers (its MMA thread is the only
