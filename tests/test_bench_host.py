@@ -74,3 +74,12 @@ def test_reference_arm_line():
     assert line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_roofline_peak_choice():
+    """A short timed region is measured against the burst tensor rate; only a
+    region of seconds (where the GPU reaches its power cap) against the
+    sustained one."""
+    assert bench.roof_peak(0.11, 1943.1, 1721.2) == ("bf16_tflops", 1943.1)
+    assert bench.roof_peak(bench.SUSTAINED_AFTER_S - 1e-3, 1943.1, 1721.2)[1] == 1943.1
+    assert bench.roof_peak(5.0, 1943.1, 1721.2) == ("bf16_tflops_sustained", 1721.2)
