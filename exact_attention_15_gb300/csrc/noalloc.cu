@@ -12,7 +12,6 @@
 // exits. The entry point allocates nothing, neither directly nor through a
 // library routine.
 #include <cstdint>
-#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -23,24 +22,22 @@ namespace {
 // Every GPU that loads this library holds this buffer until process exit.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kMaxDevices] = {};
-
 // Device address of the buffer on the current device. In host code the array's
 // name only stands in for the symbol; the real address comes from the runtime,
-// looked up once per device with that device current.
+// with the device current. It is looked up on every call rather than cached:
+// the lookup allocates nothing and is cheap, and a cached address would go stale
+// if the device's context were torn down and created again (cudaDeviceReset),
+// which reloads the library's device code and may move the buffer. The first
+// lookup on a device loads the library's device code there (this is where the
+// buffer comes into existence), so make the first call on a device before any
+// stream capture.
 int noalloc_scratch(void** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_NO_DEVICE;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return ATTN_ERR_CUDA;
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return ATTN_ERR_NO_DEVICE;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+    return ATTN_ERR_CUDA;
+  *out = p;
   return ATTN_OK;
 }
 
