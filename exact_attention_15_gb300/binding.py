@@ -22,7 +22,7 @@ ATTN_STATUS = {
     0: "ATTN_OK", 1: "ATTN_ERR_NULL_PTR", 2: "ATTN_ERR_ALIGNMENT", 3: "ATTN_ERR_UNSUPPORTED_HEADDIM",
     4: "ATTN_ERR_BAD_SHAPE", 5: "ATTN_ERR_GQA_RATIO", 6: "ATTN_ERR_CAUSAL_SHAPE",
     7: "ATTN_ERR_WORKSPACE", 8: "ATTN_ERR_CUDA", 9: "ATTN_ERR_TIMEOUT", 10: "ATTN_ERR_NO_DEVICE",
-    11: "ATTN_ERR_UNSUPPORTED_DEVICE",
+    11: "ATTN_ERR_UNSUPPORTED_DEVICE", 12: "ATTN_ERR_SEQLENS",
 }
 
 # name -> (restype, argtypes)
@@ -34,6 +34,9 @@ _SIGS = {
     "attn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
                       ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
+    "attn_bwd_dims_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I, _I, _I]),
+    "attn_bwd_dims": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P,
+                           ctypes.c_float, _I, _P, ctypes.c_size_t, _P]),
     "attn_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
                               ctypes.c_float, _I, _P]),
     "attn_check": (_I, [_P]),
@@ -51,7 +54,7 @@ _SIGS = {
 
 KERNEL_NAMES = {1: "attn_fwd_kernel", 2: "attn_bwd_pre_kernel", 3: "attn_bwd_main_kernel",
                 4: "attn_bwd_post_kernel", 5: "exp2_probe_kernel", 6: "stall_probe_kernel",
-                7: "fwd_plan_kernel", 8: "attn_fwd_pair_kernel"}
+                7: "fwd_plan_kernel", 8: "attn_fwd_pair_kernel", 9: "attn_bwd_main_kernel_pass2"}
 FAULT_NONE = 0
 FAULT_SKIP_DQ_RELEASE = 1
 BWD_ONE_CTA = 0
@@ -117,6 +120,18 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H_q, H_kv, N_q, N_k, d, causa
     return load().attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H_q, H_kv, N_q, N_k, d,
                            int(causal), seqlens, float(scale), int(deterministic), workspace,
                            workspace_bytes, stream)
+
+
+def attn_bwd_dims_workspace_bytes(B, H_q, H_kv, N_q, N_k, d_qk, d_v, varlen, deterministic) -> int:
+    return load().attn_bwd_dims_workspace_bytes(B, H_q, H_kv, N_q, N_k, d_qk, d_v, int(varlen),
+                                                int(deterministic))
+
+
+def attn_bwd_dims(q, k, v, o, lse, dout, dq, dk, dv, B, H_q, H_kv, N_q, N_k, d_qk, d_v, causal,
+                  seqlens, scale, deterministic, workspace, workspace_bytes, stream) -> int:
+    return load().attn_bwd_dims(q, k, v, o, lse, dout, dq, dk, dv, B, H_q, H_kv, N_q, N_k, d_qk,
+                                d_v, int(causal), seqlens, float(scale), int(deterministic),
+                                workspace, workspace_bytes, stream)
 
 
 def attn_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, H_q, H_kv, N_q, N_k, d, causal,
@@ -224,7 +239,7 @@ def _shape(q, k, cu_seqlens):
     return B, H_q, k.shape[2], N_q, k.shape[1], d
 
 
-def _check_inputs(q, k, v, cu_seqlens, d_v_equal=False):
+def _check_inputs(q, k, v, cu_seqlens):
     """Shapes first (so that a mismatch is reported as such), then dtype, device
     and layout: the C ABI takes sizes from q and k only, so v must match them."""
     import torch
@@ -240,8 +255,6 @@ def _check_inputs(q, k, v, cu_seqlens, d_v_equal=False):
         raise ValueError(f"q and k head dimensions differ: {q.shape[-1]} vs {k.shape[-1]}")
     if nd == 4 and k.shape[0] != q.shape[0]:
         raise ValueError(f"q and k batch sizes differ: {q.shape[0]} vs {k.shape[0]}")
-    if d_v_equal and v.shape[-1] != q.shape[-1]:
-        raise ValueError("the backward pass needs equal query/key and value head dimensions")
     for name, t in (("q", q), ("k", k), ("v", v)):
         if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
@@ -301,27 +314,33 @@ def forward(q, k, v, scale=None, causal=False, cu_seqlens=None, out=None, lse=No
 
 def backward(q, k, v, o, lse, dout, scale=None, causal=False, cu_seqlens=None,
              deterministic=False, workspace=None):
-    """Returns (dq, dk, dv). The workspace is allocated with torch unless given."""
+    """Returns (dq, dk, dv): dq like q, dk like k, dv like v (q and k have d_qk
+    columns, v, o and dout d_v). The workspace is allocated with torch unless
+    given. The default scale is 1/sqrt(d_qk)."""
     import torch
-    _check_inputs(q, k, v, cu_seqlens, d_v_equal=True)
+    _check_inputs(q, k, v, cu_seqlens)
     B, H_q, H_kv, N_q, N_k, d = _shape(q, k, cu_seqlens)
+    d_v = v.shape[-1]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    _check_tensor("o", o, q.shape, torch.bfloat16, q.device)
-    _check_tensor("dout", dout, q.shape, torch.bfloat16, q.device)
+    o_shape = q.shape[:-1] + (d_v,)
+    _check_tensor("o", o, o_shape, torch.bfloat16, q.device)
+    _check_tensor("dout", dout, o_shape, torch.bfloat16, q.device)
     _check_tensor("lse", lse, _lse_shape(B, H_q, N_q, cu_seqlens), torch.float32, q.device)
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
-    nbytes = attn_bwd_workspace_bytes(B, H_q, H_kv, N_q, N_k, d, cu_seqlens is not None, deterministic)
+    nbytes = attn_bwd_dims_workspace_bytes(B, H_q, H_kv, N_q, N_k, d, d_v, cu_seqlens is not None,
+                                           deterministic)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
     elif not workspace.is_contiguous() or workspace.device != q.device:
         raise ValueError("workspace must be a contiguous tensor on q's device")
     cu_ptr = cu_seqlens.data_ptr() if cu_seqlens is not None else None
-    _check(attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                    dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                    B, H_q, H_kv, N_q, N_k, d, causal, cu_ptr, scale, deterministic,
-                    workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr()),
-           "attn_bwd")
+    _check(attn_bwd_dims(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                         dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                         B, H_q, H_kv, N_q, N_k, d, d_v, causal, cu_ptr, scale, deterministic,
+                         workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                         _stream_ptr()),
+           "attn_bwd_dims")
     return dq, dk, dv

@@ -25,8 +25,8 @@ cudaError_t launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUte
 cudaError_t launch_attn_fwd_pair(const CUtensorMap& tq, const CUtensorMap& tk_half,
                                  const CUtensorMap& tv, const FwdParams& p, dim3 grid,
                                  cudaStream_t stream);
-cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int H_q, int pair_heads, int* seq_order,
-                            int* tile_start, cudaStream_t stream);
+cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int T, int H_q, int pair_heads,
+                            int* seq_order, int* tile_start, int* err, cudaStream_t stream);
 cudaError_t launch_exp2_probe(const float* x, float* y, int n, int mode, cudaStream_t stream);
 cudaError_t launch_stall_probe(int* err, long long limit, cudaStream_t stream);
 cudaError_t launch_attn_bwd(const BwdParams& p, const CUtensorMap* maps, cudaStream_t stream,
@@ -463,8 +463,12 @@ bool bwd_uses_pairs(int d) {
 }
 
 // The workspace size does not depend on `pairs` (only the work count does).
+// `d` is the query/key head dimension (the width of the dQ accumulator); a
+// query/key head dimension above 128 takes two passes of the main kernel, each
+// with its own ordering semaphores in deterministic mode.
 bool bwd_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d, bool varlen, bool det,
               bool pairs, BwdPlan* pl) {
+  const int passes = d > 128 ? 2 : 1;
   // work items: key tiles of 128 rows, or key pairs of 256 rows (one per CTA
   // pair)
   const long long kt = pairs ? 256 : 128;
@@ -477,11 +481,12 @@ bool bwd_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d, bool varlen, bo
     pl->slots = static_cast<long long>(B) * ((N_q + 127) / 128);
     pl->n_work = static_cast<long long>(B) * H_kv * ((N_k + kt - 1) / kt);
   }
-  if (pl->n_work > 0x7fffffffll || pl->slots * H_q > 0x7ffffffell) return false;
+  if (pl->n_work > 0x7fffffffll || (pl->slots * H_q + 1) * passes > 0x7fffffffll) return false;
   pl->acc_off = 0;
   pl->dvec_off = align256(static_cast<size_t>(pl->rows_q) * H_q * d * 4);
   pl->sem_off = pl->dvec_off + align256(static_cast<size_t>(pl->rows_q) * H_q * 4);
-  pl->total = pl->sem_off + (det ? align256(static_cast<size_t>(pl->slots * H_q + 1) * 4) : 0);
+  pl->total = pl->sem_off +
+              (det ? align256(static_cast<size_t>(pl->slots * H_q + 1) * passes * 4) : 0);
   return true;
 }
 
@@ -542,6 +547,7 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_TIMEOUT: return "device-side wait timed out";
     case ATTN_ERR_NO_DEVICE: return "no usable CUDA device";
     case ATTN_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103 (GB300 class)";
+    case ATTN_ERR_SEQLENS: return "cu_seqlens is not 0, non-decreasing, ..., N_q";
     default: return "unknown status";
   }
 }
@@ -644,7 +650,7 @@ int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* l
     if ((st = plan_buffer(dev, cs, B, &pb)) != ATTN_OK) return st;
     int* order = pb.ptr;
     int* start = order + pb.cap;
-    if (launch_fwd_plan(seqlens, B, H_q, p.pair_heads, order, start, cs) != cudaSuccess)
+    if (launch_fwd_plan(seqlens, B, N_q, H_q, p.pair_heads, order, start, err, cs) != cudaSuccess)
       return ATTN_ERR_CUDA;
     p.seq_order = order;
     p.tile_start = start;
@@ -670,12 +676,26 @@ int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* l
 
 size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int N_q, int N_k, int d, int varlen,
                                 int deterministic) {
+  if (d != 64 && d != 128) return 0;
+  return attn_bwd_dims_workspace_bytes(B, H_q, H_kv, N_q, N_k, d, d, varlen, deterministic);
+}
+
+namespace {
+bool bwd_dims_supported(int d_qk, int d_v) {
+  return (d_qk == 64 && d_v == 64) || (d_qk == 128 && d_v == 128) || (d_qk == 192 && d_v == 128);
+}
+}  // namespace
+
+size_t attn_bwd_dims_workspace_bytes(int B, int H_q, int H_kv, int N_q, int N_k, int d_qk, int d_v,
+                                     int varlen, int deterministic) {
+  if (!bwd_dims_supported(d_qk, d_v)) return 0;
   Shape s;
-  if (check_shape(B, H_q, H_kv, N_q, N_k, d, 0, varlen ? reinterpret_cast<const int*>(16) : nullptr,
+  if (check_shape(B, H_q, H_kv, N_q, N_k, d_v, 0, varlen ? reinterpret_cast<const int*>(16) : nullptr,
                   &s) != ATTN_OK)
     return 0;
+  if (static_cast<long long>(B) * (N_q + N_k) * H_q * d_qk > (1ll << 46)) return 0;
   BwdPlan pl;
-  if (!bwd_plan(B, H_q, H_kv, N_q, N_k, d, varlen != 0, deterministic != 0, false, &pl)) return 0;
+  if (!bwd_plan(B, H_q, H_kv, N_q, N_k, d_qk, varlen != 0, deterministic != 0, false, &pl)) return 0;
   return pl.total;
 }
 
@@ -683,9 +703,22 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              const void* dout, void* dq, void* dk, void* dv, int B, int H_q, int H_kv, int N_q,
              int N_k, int d, int causal, const int* seqlens, float scale, int deterministic,
              void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED_HEADDIM;
+  return attn_bwd_dims(q, k, v, o, lse, dout, dq, dk, dv, B, H_q, H_kv, N_q, N_k, d, d, causal,
+                       seqlens, scale, deterministic, workspace, workspace_bytes, stream);
+}
+
+int attn_bwd_dims(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, int B, int H_q, int H_kv,
+                  int N_q, int N_k, int d_qk, int d_v, int causal, const int* seqlens, float scale,
+                  int deterministic, void* workspace, size_t workspace_bytes,
+                  attn_stream_t stream) {
+  if (!bwd_dims_supported(d_qk, d_v)) return ATTN_ERR_UNSUPPORTED_HEADDIM;
   Shape s;
-  int st = check_shape(B, H_q, H_kv, N_q, N_k, d, causal, seqlens, &s);
+  int st = check_shape(B, H_q, H_kv, N_q, N_k, d_v, causal, seqlens, &s);
   if (st != ATTN_OK) return st;
+  // element-count bound of check_shape, with the wider head dimension
+  if (static_cast<long long>(B) * (N_q + N_k) * H_q * d_qk > (1ll << 46)) return ATTN_ERR_BAD_SHAPE;
   const bool has_q = B > 0 && N_q > 0, has_k = B > 0 && N_k > 0;
   if ((has_q && (!q || !o || !lse || !dout || !dq)) || (has_k && (!k || !v || !dk || !dv)))
     return ATTN_ERR_NULL_PTR;
@@ -695,8 +728,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
       (seqlens && (reinterpret_cast<uintptr_t>(seqlens) & 3u)))
     return ATTN_ERR_ALIGNMENT;
   BwdPlan pl;
-  const bool pairs = bwd_uses_pairs(d);
-  if (!bwd_plan(B, H_q, H_kv, N_q, N_k, d, seqlens != nullptr, deterministic != 0, pairs, &pl))
+  const bool pairs = d_qk == d_v && bwd_uses_pairs(d_qk);
+  if (!bwd_plan(B, H_q, H_kv, N_q, N_k, d_qk, seqlens != nullptr, deterministic != 0, pairs, &pl))
     return ATTN_ERR_BAD_SHAPE;
   if (B == 0) return ATTN_OK;
   const bool empty = (N_q == 0 || N_k == 0);
@@ -707,29 +740,32 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   int* err = nullptr;
   if ((st = device_setup(dev, &err)) != ATTN_OK) return st;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  const size_t q_bytes = static_cast<size_t>(pl.rows_q) * H_q * d * 2;
-  const size_t k_bytes = static_cast<size_t>(s.varlen ? N_k : static_cast<long long>(B) * N_k) * H_kv * d * 2;
+  const size_t k_rows = static_cast<size_t>(s.varlen ? N_k : static_cast<long long>(B) * N_k);
+  const size_t q_bytes = static_cast<size_t>(pl.rows_q) * H_q * d_qk * 2;
+  const size_t k_bytes = k_rows * H_kv * d_qk * 2;
+  const size_t v_bytes = k_rows * H_kv * d_v * 2;
   if (empty) {
     // no query rows: no key gradient; no keys: every row sees nothing
     if ((q_bytes && cudaMemsetAsync(dq, 0, q_bytes, cs) != cudaSuccess) ||
         (k_bytes && cudaMemsetAsync(dk, 0, k_bytes, cs) != cudaSuccess) ||
-        (k_bytes && cudaMemsetAsync(dv, 0, k_bytes, cs) != cudaSuccess))
+        (v_bytes && cudaMemsetAsync(dv, 0, v_bytes, cs) != cudaSuccess))
       return ATTN_ERR_CUDA;
     return ATTN_OK;
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  // q, k, v, dO (128-row boxes), the fp32 dQ accumulator (128-row boxes, 64 on
-  // CTA pairs), and at d = 128 q and dO with 64-row boxes
+  // q, k (d_qk), v, dO (d_v) with 128-row boxes, the fp32 dQ accumulator
+  // (d_qk; 128-row boxes, 64 on CTA pairs), and on CTA pairs q and dO with
+  // 64-row boxes
   CUtensorMap maps[7];
-  if (encode_rows_map(&maps[0], q, d, H_q, s.q_rows, s.q_batch) != ATTN_OK ||
-      encode_rows_map(&maps[1], k, d, H_kv, s.k_rows, s.q_batch) != ATTN_OK ||
-      encode_rows_map(&maps[2], v, d, H_kv, s.k_rows, s.q_batch) != ATTN_OK ||
-      encode_rows_map(&maps[3], dout, d, H_q, s.q_rows, s.q_batch) != ATTN_OK ||
-      encode_rows_map(&maps[4], ws + pl.acc_off, d, H_q, s.q_rows, s.q_batch, true,
+  if (encode_rows_map(&maps[0], q, d_qk, H_q, s.q_rows, s.q_batch) != ATTN_OK ||
+      encode_rows_map(&maps[1], k, d_qk, H_kv, s.k_rows, s.q_batch) != ATTN_OK ||
+      encode_rows_map(&maps[2], v, d_v, H_kv, s.k_rows, s.q_batch) != ATTN_OK ||
+      encode_rows_map(&maps[3], dout, d_v, H_q, s.q_rows, s.q_batch) != ATTN_OK ||
+      encode_rows_map(&maps[4], ws + pl.acc_off, d_qk, H_q, s.q_rows, s.q_batch, true,
                       pairs ? 64u : 128u) != ATTN_OK)
     return ATTN_ERR_CUDA;
-  if (pairs && (encode_rows_map(&maps[5], q, d, H_q, s.q_rows, s.q_batch, false, 64u) != ATTN_OK ||
-                encode_rows_map(&maps[6], dout, d, H_q, s.q_rows, s.q_batch, false, 64u) != ATTN_OK))
+  if (pairs && (encode_rows_map(&maps[5], q, d_qk, H_q, s.q_rows, s.q_batch, false, 64u) != ATTN_OK ||
+                encode_rows_map(&maps[6], dout, d_v, H_q, s.q_rows, s.q_batch, false, 64u) != ATTN_OK))
     return ATTN_ERR_CUDA;
 
   BwdParams p;
@@ -739,7 +775,9 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   p.dvec = reinterpret_cast<float*>(ws + pl.dvec_off);
   p.sem = deterministic ? reinterpret_cast<int*>(ws + pl.sem_off) : nullptr;
   p.cu_seqlens = seqlens;
-  p.B = B; p.H_q = H_q; p.H_kv = H_kv; p.N_q = N_q; p.N_k = N_k; p.group = H_q / H_kv; p.d = d;
+  p.B = B; p.H_q = H_q; p.H_kv = H_kv; p.N_q = N_q; p.N_k = N_k; p.group = H_q / H_kv;
+  p.d = d_qk;
+  p.d_v = d_v;
   p.causal = causal ? 1 : 0;
   p.deterministic = deterministic ? 1 : 0;
   p.n_nblocks = 0;
@@ -784,7 +822,7 @@ int attn_check(attn_stream_t stream) {
     const int zero = 0;
     if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
       return ATTN_ERR_CUDA;
-    return ATTN_ERR_TIMEOUT;
+    return h == kErrSeqlens ? ATTN_ERR_SEQLENS : ATTN_ERR_TIMEOUT;
   }
   return ATTN_OK;
 }

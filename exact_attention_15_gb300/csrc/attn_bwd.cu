@@ -40,20 +40,32 @@
 
 namespace attn {
 
-template <int D>
+// Shared-memory and TMEM plan of the main kernel. Q and K rows have DQK
+// columns, V and dO rows DV; every tile is stored as 128-row x 64-column (16 KB)
+// 128-byte-swizzled blocks. A pass computes dK and dQ for the query/key head
+// columns [C0, C0 + NC) (all of them when DQK <= 128; DQK = 192 takes two
+// passes, 0-127 and 128-191, because dV, dK, S^T and dP^T / dQ of 192 columns
+// need 640 of the 512 TMEM columns), and dV in the pass with C0 = 0.
+template <int DQK, int DV, int NC>
 struct BwdCfg {
-  static constexpr int kTileBytes = kTileM * D * 2;  // one 128-row bf16 tile of Q, dO, K or V
+  static_assert(DQK % 64 == 0 && DV % 64 == 0 && DV <= 128 && NC <= 128, "head dimensions");
+  static constexpr int kQKBytes = kTileM * DQK * 2;  // one 128-row bf16 tile of Q or K
+  static constexpr int kVBytes = kTileM * DV * 2;    // one 128-row bf16 tile of V or dO
+  // two Q stages fit next to everything else up to 128 columns; at 192 one
+  static constexpr int kQStages = DQK <= 128 ? 2 : 1;
   static constexpr int kKOff = 0;
-  static constexpr int kVOff = kKOff + kTileBytes;
-  static constexpr int kQOff = kVOff + kTileBytes;             // 2 stages
-  static constexpr int kdOOff = kQOff + 2 * kTileBytes;        // 1 stage (reloaded once dV is done)
-  static constexpr int kdSOff = kdOOff + kTileBytes;           // 128 x 128 bf16
-  static constexpr int kdQOff = kdSOff + 128 * 128 * 2;        // 2 x (128 rows x 32 fp32) staging
-  static constexpr int kStatOff = kdQOff + 2 * 16384;          // per Q stage: lse2[128], D[128]
-  static constexpr int kBarOff = kStatOff + 2 * 2 * 128 * 4;
+  static constexpr int kVOff = kKOff + kQKBytes;
+  static constexpr int kQOff = kVOff + kVBytes;                 // kQStages stages
+  static constexpr int kdOOff = kQOff + kQStages * kQKBytes;    // 1 stage (reloaded once dV is done)
+  static constexpr int kdSOff = kdOOff + kVBytes;               // 128 x 128 bf16
+  static constexpr int kdQOff = kdSOff + 128 * 128 * 2;         // 2 x (128 rows x 32 fp32) staging
+  static constexpr int kStatOff = kdQOff + 2 * 16384;           // per Q stage: lse2[128], D[128]
+  static constexpr int kBarOff = kStatOff + kQStages * 2 * 128 * 4;
   static constexpr int kSmemBytes = kBarOff + 256;
-  static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
+  static constexpr uint32_t kColDV = 0, kColDK = DV, kColS = 2 * DV, kColDP = 2 * DV + 128;
   static constexpr uint32_t kTmemCols = 512;
+  static_assert(kColDK + NC <= kColS && kColDP + (NC > 128 ? NC : 128) <= kTmemCols, "TMEM plan");
+  static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
 struct BwdBars {
@@ -91,21 +103,24 @@ __device__ __forceinline__ bool decode_bwd_tile(const BwdParams& p, int idx, Bwd
     t.Lk = p.N_k;
     t.sem_base = t.b * ((p.N_q + kTileM - 1) / kTileM);
   } else {
+    // sequences in order, each clamped after the one before it (seq_span), so
+    // their query-tile slots stay within the semaphore array
     int s = 0, qslots = 0;
+    SeqSpan sp{0, 0};
     for (; s < p.B; ++s) {
-      const int L = p.cu_seqlens[s + 1] - p.cu_seqlens[s];
-      const int nk = (L + kTileN - 1) / kTileN;
+      sp = seq_span(p.cu_seqlens, s, p.N_q, sp.start + sp.len);
+      const int nk = (sp.len + kTileN - 1) / kTileN;
       if (idx < nk * p.H_kv) break;
       idx -= nk * p.H_kv;
-      qslots += (L + kTileM - 1) / kTileM;
+      qslots += (sp.len + kTileM - 1) / kTileM;
     }
     if (s >= p.B) return false;
-    const int L = p.cu_seqlens[s + 1] - p.cu_seqlens[s];
+    const int L = sp.len;
     const int nk = (L + kTileN - 1) / kTileN;
     t.j = SPT ? nk - 1 - idx % nk : idx % nk;
     t.h_kv = idx / nk;
     t.b = s;
-    t.row_base = p.cu_seqlens[s];
+    t.row_base = sp.start;
     t.batch_coord = 0;
     t.Lq = L;
     t.Lk = L;
@@ -138,7 +153,9 @@ __device__ __forceinline__ int bwd_query_tile(const BwdParams& p, const BwdTile&
 
 // ------------------------------------------------------------------ pre / post
 
-// D[row] = sum_c dO[row, c] * O[row, c]; G = d/16 lanes per (row, head).
+// D[row] = sum_c dO[row, c] * O[row, c] over the D value columns; G = D/16
+// lanes per (row, head). Zeroes the fp32 dQ accumulator (n_acc_vec4 float4s)
+// and the ints sem[0 .. n_sem].
 template <int D>
 __global__ void __launch_bounds__(256)
 attn_bwd_pre_kernel(const BwdParams p, long long n_rowheads, long long n_acc_vec4, int n_sem) {
@@ -150,6 +167,9 @@ attn_bwd_pre_kernel(const BwdParams p, long long n_rowheads, long long n_acc_vec
   for (long long i = tid; i < n_acc_vec4; i += nthreads) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (p.sem != nullptr)  // the semaphores and, after them, the work-ticket counter
     for (long long i = tid; i <= n_sem; i += nthreads) p.sem[i] = 0;
+  // an inconsistent packed-sequence offset array is reported (the main kernel
+  // clamps what it decodes, so it stays inside the tensors either way)
+  if (p.cu_seqlens != nullptr) check_cu_seqlens(p.cu_seqlens, p.B, p.N_q, p.err, tid, nthreads);
   // D: a warp handles 32 / G (row, head) pairs per step; the loop bounds are
   // uniform across the warp so the shuffles below always have every lane.
   const long long warp_id = tid >> 5;
@@ -191,7 +211,6 @@ attn_bwd_pre_kernel(const BwdParams p, long long n_rowheads, long long n_acc_vec
   }
 }
 
-template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const BwdParams p, long long n_vec8) {
   const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec8;
@@ -212,12 +231,33 @@ __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const BwdParams p, l
 
 
 
-template <int D, bool SPT>
+// dQ of a pass with 128 query/key head columns is computed transposed, dQ^T =
+// K^T dS^T (the same two shared-memory operands as dS K, A and B swapped), so
+// that TMEM lane = head column and column = query: after a 32x32b TMEM load a
+// warp holds 32 consecutive head columns of each query row, and every
+// red.global.add.f32 warp instruction covers one whole 128-byte line of the dQ
+// accumulator. That replaces the shared-memory staging of dQ (a 64 KB write
+// and a 64 KB read per query tile) in a kernel whose time is set by its
+// shared-memory traffic. Passes of 64 columns (d = 64, and the second pass at
+// d_qk = 192) would need an M = 64 MMA there and keep the staged bulk
+// reductions.
+#ifndef ATTN_BWD_DQ_T
+#define ATTN_BWD_DQ_T 0
+#endif
+
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+template <int DQK, int DV, int C0, int NC, bool SPT>
 __global__ void __launch_bounds__(512, 1)
 attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_dq, const BwdParams p, int* ticket) {
-  using Cfg = BwdCfg<D>;
+  using Cfg = BwdCfg<DQK, DV, NC>;
+  constexpr bool kDoDV = C0 == 0;          // this pass also accumulates dV
+  constexpr int kQS = Cfg::kQStages;
+  constexpr bool kDqT = ATTN_BWD_DQ_T && NC == 128;  // dQ^T in TMEM, reduced from registers
   extern __shared__ __align__(1024) uint8_t smem[];
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + Cfg::kBarOff);
 
@@ -276,28 +316,28 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           tma_prefetch_desc(&tm_q);
           tma_prefetch_desc(&tm_do);
           const uint32_t kvb = smem_addr(&bars->kv_full);
-          mbar_arrive_expect_tx(kvb, 2 * Cfg::kTileBytes);
-          for (int hf = 0; hf < D / 64; ++hf) {
+          mbar_arrive_expect_tx(kvb, Cfg::kQKBytes + Cfg::kVBytes);
+          for (int hf = 0; hf < DQK / 64; ++hf)
             tma_load_4d(smem_addr(smem + Cfg::kKOff) + hf * 16384, &tm_k, kvb, hf * 64, t.h_kv,
                         t.row_base + t.j * kTileN, t.batch_coord);
+          for (int hf = 0; hf < DV / 64; ++hf)
             tma_load_4d(smem_addr(smem + Cfg::kVOff) + hf * 16384, &tm_v, kvb, hf * 64, t.h_kv,
                         t.row_base + t.j * kTileN, t.batch_coord);
-          }
         }
         float* stat = reinterpret_cast<float*>(smem + Cfg::kStatOff);
         for (int it = 0; it < n_it; ++it) {
-          const int stage = it & 1;
+          const int stage = it % kQS;
           const int h = t.h_kv * p.group + it / n_per_head;
           const int i = bwd_query_tile<SPT>(p, t, it % n_per_head);
-          if (!mbar_wait(smem_addr(&bars->q_empty[stage]), ((it >> 1) & 1) ^ 1, lim)) {
+          if (!mbar_wait(smem_addr(&bars->q_empty[stage]), ((it / kQS) & 1) ^ 1, lim)) {
             record_error(p.err, kErrTimeout);
             break;
           }
           const uint32_t fb = smem_addr(&bars->q_full[stage]);
           if (lane == 0) {
-            mbar_expect_tx(fb, Cfg::kTileBytes);
-            for (int hf = 0; hf < D / 64; ++hf)
-              tma_load_4d(smem_addr(smem + Cfg::kQOff + stage * Cfg::kTileBytes) + hf * 16384, &tm_q,
+            mbar_expect_tx(fb, Cfg::kQKBytes);
+            for (int hf = 0; hf < DQK / 64; ++hf)
+              tma_load_4d(smem_addr(smem + Cfg::kQOff + stage * Cfg::kQKBytes) + hf * 16384, &tm_q,
                           fb, hf * 64, h, t.row_base + i * kTileM, t.batch_coord);
           }
           // LSE (to log2 units) and D for the 128 rows of this query tile; rows
@@ -328,8 +368,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           }
           if (lane == 0) {
             const uint32_t db = smem_addr(&bars->do_full);
-            mbar_arrive_expect_tx(db, Cfg::kTileBytes);
-            for (int hf = 0; hf < D / 64; ++hf)
+            mbar_arrive_expect_tx(db, Cfg::kVBytes);
+            for (int hf = 0; hf < DV / 64; ++hf)
               tma_load_4d(smem_addr(smem + Cfg::kdOOff) + hf * 16384, &tm_do, db, hf * 64, h,
                           t.row_base + i * kTileM, t.batch_coord);
           }
@@ -338,91 +378,110 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       }
     } else if (warp == 1) {
       // ------------------------------------------------------- MMA issuer
-      // Issue order per query tile i (S_{i+1} goes ahead of dK_i / dQ_i so the
-      // tensor core has work while the compute warps turn dP_i into dS_i and
-      // S_{i+1} into P_{i+1}):
+      // Issue order per query tile i with two Q stages (S_{i+1} goes ahead of
+      // dK_i / dQ_i so the tensor core has work while the compute warps turn
+      // dP_i into dS_i and S_{i+1} into P_{i+1}):
       //   S_0, dP_0 | dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1} | ...
+      // With one Q stage (DQK = 192) Q_{i+1} can only load once dK_i, the last
+      // reader of Q_i, is done:
+      //   S_0, dP_0 | dV_i, dK_i, dQ_i, S_{i+1}, dP_{i+1} | ...
+      // A pass without dV skips it; dK and dQ cover the pass's NC columns.
       if (lane == 0 && n_it > 0) {
         constexpr uint32_t kIdSS = make_idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
-        constexpr uint32_t kIdKM = make_idesc_bf16(128, D, 0, 1);    // dV, dK: B MN-major
-        constexpr uint32_t kIdDQ = make_idesc_bf16(128, D, 1, 1);    // dQ: A and B MN-major
+        constexpr uint32_t kIdDV = make_idesc_bf16(128, DV, 0, 1);   // dV: B MN-major
+        constexpr uint32_t kIdDK = make_idesc_bf16(128, NC, 0, 1);   // dK: B MN-major
+        constexpr uint32_t kIdDQ = make_idesc_bf16(128, NC, 1, 1);   // dQ: A and B MN-major
+        constexpr uint32_t kIdDQT = make_idesc_bf16(NC, 128, 1, 1);  // dQ^T: A and B MN-major
         // Descriptors are built once; each MMA only adds a compile-time byte
         // offset (>> 4) to the start-address field, which keeps the single
-        // issuing thread ahead of the tensor core. Every tile is a
-        // 128-byte-swizzled [rows x 64] block pair that reads as K-major (lbo
-        // unused) or MN-major (lbo = 16 KB between the 64-column blocks).
+        // issuing thread ahead of the tensor core. Every tile is made of
+        // 128-byte-swizzled [rows x 64] blocks that read as K-major (lbo
+        // unused) or MN-major (lbo = 16 KB between the 64-column blocks); the
+        // pass's columns of Q and K start at block C0 / 64.
+        constexpr uint32_t kC0Blk = (C0 / 64) * (16384 >> 4);
         const uint32_t k_base = smem_addr(smem + Cfg::kKOff);
         const uint32_t v_base = smem_addr(smem + Cfg::kVOff);
         const uint32_t ds_base = smem_addr(smem + Cfg::kdSOff);
         const uint64_t k_km = make_sdesc_sw128(k_base, 16, 1024);
-        const uint64_t k_mn = make_sdesc_sw128(k_base, 16384, 1024);
+        const uint64_t k_mn = make_sdesc_sw128(k_base, 16384, 1024) + kC0Blk;
         const uint64_t v_km = make_sdesc_sw128(v_base, 16, 1024);
         const uint64_t q_km = make_sdesc_sw128(smem_addr(smem + Cfg::kQOff), 16, 1024);
-        const uint64_t q_mn = make_sdesc_sw128(smem_addr(smem + Cfg::kQOff), 16384, 1024);
+        const uint64_t q_mn = make_sdesc_sw128(smem_addr(smem + Cfg::kQOff), 16384, 1024) + kC0Blk;
         const uint64_t do_km = make_sdesc_sw128(smem_addr(smem + Cfg::kdOOff), 16, 1024);
         const uint64_t do_mn = make_sdesc_sw128(smem_addr(smem + Cfg::kdOOff), 16384, 1024);
         const uint64_t ds_km = make_sdesc_sw128(ds_base, 16, 1024);
         const uint64_t ds_mn = make_sdesc_sw128(ds_base, 16384, 1024);
-        constexpr uint32_t kStageStep = Cfg::kTileBytes >> 4;
+        constexpr uint32_t kStageStep = Cfg::kQKBytes >> 4;
         auto koff = [](int kk) { return static_cast<uint32_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4); };
         auto issue_s = [&](int it) {  // S^T = K Q^T
-          const uint64_t qb = q_km + (it & 1) * kStageStep;
+          const uint64_t qb = q_km + (it % kQS) * kStageStep;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
+          for (int kk = 0; kk < DQK / 16; ++kk)
             mma_ss(tmem + Cfg::kColS, k_km + koff(kk), qb + koff(kk), kIdSS, kk > 0);
           mma_commit(smem_addr(&bars->s_full));
         };
         auto issue_dp = [&](int) {  // dP^T = V dO^T
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
+          for (int kk = 0; kk < DV / 16; ++kk)
             mma_ss(tmem + Cfg::kColDP, v_km + koff(kk), do_km + koff(kk), kIdSS, kk > 0);
           mma_commit(smem_addr(&bars->dp_full));
         };
-        bool ok = mbar_wait(smem_addr(&bars->kv_full), 0, lim);
-        if (ok) ok = mbar_wait(smem_addr(&bars->q_full[0]), 0, lim);
-        if (ok) {
+        auto wait_issue_s = [&](int it) {  // S^T of tile `it` once its Q is in
+          if (!mbar_wait(smem_addr(&bars->q_full[it % kQS]), (it / kQS) & 1, lim)) return false;
           tc_fence_after();
-          issue_s(0);
-        }
+          issue_s(it);
+          return true;
+        };
+        bool ok = mbar_wait(smem_addr(&bars->kv_full), 0, lim);
+        if (ok) ok = wait_issue_s(0);
         if (ok) ok = mbar_wait(smem_addr(&bars->do_full), 0, lim);
         if (ok) {
           tc_fence_after();
           issue_dp(0);
         }
         for (int it = 0; ok && it < n_it; ++it) {
-          const int stage = it & 1;
+          const int stage = it % kQS;
           // dV += P^T dO  (P^T from TMEM)
           if (!(ok = mbar_wait(smem_addr(&bars->p_ready), it & 1, lim))) break;
           tc_fence_after();
-          // P^T for queries [0, 64) sits in S^T columns [0, 32), for queries
-          // [64, 128) in columns [64, 96); each MMA reads one 16-query slice
+          if constexpr (kDoDV) {
+            // P^T for queries [0, 64) sits in S^T columns [0, 32), for queries
+            // [64, 128) in columns [64, 96); each MMA reads one 16-query slice
 #pragma unroll
-          for (int kk = 0; kk < kTileM / 16; ++kk)
-            mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
-                   do_mn + kk * (2048 >> 4), kIdKM, (it > 0 || kk > 0));
+            for (int kk = 0; kk < kTileM / 16; ++kk)
+              mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
+                     do_mn + kk * (2048 >> 4), kIdDV, (it > 0 || kk > 0));
+          }
           mma_commit(smem_addr(&bars->do_empty));  // dO_i fully read: the next one may load
           // S^T of the next query tile into the same TMEM columns (the MMAs run
           // in issue order, so dV has read P^T before they are overwritten)
-          if (it + 1 < n_it) {
-            if (!(ok = mbar_wait(smem_addr(&bars->q_full[(it + 1) & 1]), ((it + 1) >> 1) & 1, lim))) break;
-            tc_fence_after();
-            issue_s(it + 1);
-          }
+          if (kQS == 2 && it + 1 < n_it && !(ok = wait_issue_s(it + 1))) break;
           // dK += dS^T Q (dS^T: the shared-memory dS buffer read K-major);
           // dQ = dS K (the same buffer read MN-major)
           if (!(ok = mbar_wait(smem_addr(&bars->ds_ready), it & 1, lim))) break;
           tc_fence_after();
-          const uint64_t qmn = q_mn + (it & 1) * kStageStep;
+          const uint64_t qmn = q_mn + stage * kStageStep;
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk)
-            mma_ss(tmem + Cfg::kColDK, ds_km + koff(kk), qmn + kk * (2048 >> 4), kIdKM,
+            mma_ss(tmem + Cfg::kColDK, ds_km + koff(kk), qmn + kk * (2048 >> 4), kIdDK,
                    (it > 0 || kk > 0));
+          if constexpr (kQS == 1) mma_commit(smem_addr(&bars->q_empty[0]));  // Q_i fully read
+          if constexpr (kDqT) {
+            // dQ^T = K^T dS^T: A = the pass's K columns (MN-major, M = head
+            // columns), B = dS (MN-major, N = queries), K-steps over keys
 #pragma unroll
-          for (int kk = 0; kk < kTileN / 16; ++kk)
-            mma_ss(tmem + Cfg::kColDP, ds_mn + kk * (2048 >> 4), k_mn + kk * (2048 >> 4), kIdDQ,
-                   kk > 0);
+            for (int kk = 0; kk < kTileN / 16; ++kk)
+              mma_ss(tmem + Cfg::kColDP, k_mn + kk * (2048 >> 4), ds_mn + kk * (2048 >> 4), kIdDQT,
+                     kk > 0);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kTileN / 16; ++kk)
+              mma_ss(tmem + Cfg::kColDP, ds_mn + kk * (2048 >> 4), k_mn + kk * (2048 >> 4), kIdDQ,
+                     kk > 0);
+          }
           mma_commit(smem_addr(&bars->dq_full));  // covers every earlier MMA, dV included
-          mma_commit(smem_addr(&bars->q_empty[stage]));
+          if constexpr (kQS == 2) mma_commit(smem_addr(&bars->q_empty[stage]));
+          if (kQS == 1 && it + 1 < n_it && !(ok = wait_issue_s(it + 1))) break;
           // dP^T of the next tile reuses the dQ columns once dQ_i has been read out
           if (it + 1 < n_it) {
             if (!(ok = mbar_wait(smem_addr(&bars->dq_free), it & 1, lim))) break;
@@ -450,9 +509,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     uint8_t* ds_blk = smem + Cfg::kdSOff + c * 16384;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int stage = it & 1;
+      const int stage = it % kQS;
       const int i = bwd_query_tile<SPT>(p, t, it % n_per_head);
-      if (!(ok = mbar_wait(smem_addr(&bars->q_full[stage]), (it >> 1) & 1, lim))) break;
+      if (!(ok = mbar_wait(smem_addr(&bars->q_full[stage]), (it / kQS) & 1, lim))) break;
       if (!(ok = mbar_wait(smem_addr(&bars->s_full), it & 1, lim))) break;
       tc_fence_after();
       const float* lse2 = stat + stage * 256 + 64 * c;
@@ -523,7 +582,8 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
     if (!ok) record_error(p.err, kErrTimeout);
     // --------------------------------------------------------- dK / dV epilogue
-    // warpgroup c writes columns [c d/2, (c+1) d/2) of this key row
+    // warpgroup c writes the pass's dK columns [C0 + c NC/2, C0 + (c+1) NC/2) and,
+    // in the pass with dV, dV columns [c DV/2, (c+1) DV/2) of this key row
     bool have = ok && n_it > 0;
     if (have) {
       // the last dq_full commit covers every MMA, the last dV included
@@ -535,19 +595,19 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       // every lane takes part in the (warp-collective) TMEM loads; only rows
       // inside the sequence are stored
       const size_t grow = static_cast<size_t>(t.row_base) + kv;
-      const size_t off = p.cu_seqlens
-                             ? (grow * p.H_kv + t.h_kv) * D
-                             : ((static_cast<size_t>(t.b) * p.N_k + kv) * p.H_kv + t.h_kv) * D;
-      uint4* dk_row = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dk) + off);
-      uint4* dv_row = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dv) + off);
+      const size_t krow = p.cu_seqlens ? grow * p.H_kv + t.h_kv
+                                       : (static_cast<size_t>(t.b) * p.N_k + kv) * p.H_kv + t.h_kv;
+      uint4* dk_row = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dk) + krow * DQK + C0);
+      uint4* dv_row = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dv) + krow * DV);
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
+      for (int which = kDoDV ? 0 : 1; which < 2; ++which) {
         const uint32_t col = which ? Cfg::kColDK : Cfg::kColDV;
         const float mul = which ? p.scale : 1.0f;
         uint4* dst = which ? dk_row : dv_row;
+        const int half = which ? NC / 2 : DV / 2;
 #pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) {
-          const int c0 = c * (D / 2) + cc * 32;
+        for (int cc = 0; cc < half / 32; ++cc) {
+          const int c0 = c * half + cc * 32;
           uint32_t v[32];
           if (have) {
             tmem_ld32(tmem + lane_base + col + c0, v);
@@ -570,7 +630,9 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
   } else {
     regs_inc<144>();
-    // --------------------------------------------------------- dQ (query row r)
+    // --------------------------------------------------------- dQ
+    // thread r: query row r of the dQ_i tile, or head column C0 + r of the
+    // transposed tile (kDqT)
     const int r = tid - 384;
     const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
     bool ok = true;
@@ -579,12 +641,12 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       const int i = bwd_query_tile<SPT>(p, t, it % n_per_head);
       if (!(ok = mbar_wait(smem_addr(&bars->dq_full), it & 1, lim))) break;
       tc_fence_after();
-      uint32_t v[D];
+      uint32_t v[NC];
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc)
+      for (int cc = 0; cc < NC / 32; ++cc)
         tmem_ld32(tmem + lane_base + Cfg::kColDP + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(v + cc * 32));
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + cc * 32));
+      for (int cc = 0; cc < NC / 32; ++cc) tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + cc * 32));
       tc_fence_before();
       mbar_arrive(smem_addr(&bars->dq_free));
       int* sem = nullptr;
@@ -601,14 +663,26 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
         named_bar_sync(1, 128);
       }
-      if (p.cu_seqlens != nullptr && (i + 1) * kTileM > t.Lq) {
+      if constexpr (kDqT) {
+        // v[q] = dQ_i[q][C0 + r]: for each query row the warp adds 32
+        // consecutive floats (one 128-byte line); rows past the end of the
+        // sequence or batch entry are skipped (warp-uniform)
+        const int n_rows = min(kTileM, t.Lq - i * kTileM);
+        const size_t row0 = p.cu_seqlens ? static_cast<size_t>(t.row_base) + i * kTileM
+                                         : static_cast<size_t>(t.b) * p.N_q + i * kTileM;
+        float* dst = p.dq_acc + (row0 * p.H_q + h) * DQK + C0 + r;
+        const size_t row_step = static_cast<size_t>(p.H_q) * DQK;
+#pragma unroll
+        for (int q = 0; q < kTileM; ++q)
+          if (q < n_rows) red_add_f32(dst + q * row_step, __uint_as_float(v[q]));
+      } else if (p.cu_seqlens != nullptr && (i + 1) * kTileM > t.Lq) {
         // last tile of a packed sequence: a 128-row bulk reduction would also
         // touch the next sequence's rows, so add the valid rows one by one
         const int q = i * kTileM + r;
         if (q < t.Lq) {
-          float* dst = p.dq_acc + ((static_cast<size_t>(t.row_base) + q) * p.H_q + h) * D;
+          float* dst = p.dq_acc + ((static_cast<size_t>(t.row_base) + q) * p.H_q + h) * DQK + C0;
 #pragma unroll
-          for (int e = 0; e < D / 4; ++e)
+          for (int e = 0; e < NC / 4; ++e)
             red_add_v4(dst + 4 * e, __uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
                        __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
         }
@@ -617,7 +691,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         // one bulk tensor reduction (rows past the end of a fixed-length batch
         // entry fall outside the tensor map and are dropped)
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < NC / 32; ++cc) {
           const int buf = cc & 1;
           uint8_t* stage_buf = smem + Cfg::kdQOff + buf * 16384;
           if (r == 0) bulk_wait_group_read<1>();  // this buffer's previous reduction has read it
@@ -630,14 +704,14 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           fence_async_shared();
           named_bar_sync(1, 128);
           if (r == 0) {
-            tma_reduce_add_4d(&tm_dq, smem_addr(stage_buf), cc * 32, h, t.row_base + i * kTileM,
+            tma_reduce_add_4d(&tm_dq, smem_addr(stage_buf), C0 + cc * 32, h, t.row_base + i * kTileM,
                               t.batch_coord);
             bulk_commit_group();
           }
         }
       }
       if (p.deterministic) {
-        if (r == 0) {
+        if (!kDqT && r == 0) {
           bulk_wait_group<0>();  // our reductions are complete in global memory
           fence_async_global();
         }
@@ -649,7 +723,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (r == 0 && !skip) atomicAdd(sem, 1);
       }
     }
-    if (r == 0) bulk_wait_group<0>();  // staging buffers are read before the CTA exits
+    if (!kDqT && r == 0) bulk_wait_group<0>();  // staging buffers are read before the CTA exits
     if (!ok) record_error(p.err, kErrTimeout);
   }
   tc_fence_before();
@@ -665,51 +739,74 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 cudaError_t launch_attn_bwd_pair_main(const BwdParams& p, const CUtensorMap* maps, int n_pairs,
                                       int* ticket, cudaStream_t st);
 
-template <int D>
-static cudaError_t launch_bwd_impl(const BwdParams& p, const CUtensorMap* maps, cudaStream_t st,
-                                   long long rows_q, int n_sem, int n_work) {
-  const long long n_rowheads = rows_q * p.H_q;
-  const long long n_acc4 = n_rowheads * D / 4;
-  const int threads = 256;
-  long long want = (n_acc4 + threads - 1) / threads;
-  int blocks = static_cast<int>(want < 152 * 16 ? (want > 0 ? want : 1) : 152 * 16);
-  int slot = prof_begin(kKBwdPre, st);
-  attn_bwd_pre_kernel<D><<<blocks, threads, 0, st>>>(p, n_rowheads, n_acc4, n_sem);
-  cudaError_t e = cudaGetLastError();
-  prof_end(slot, st);
+template <int DQK, int DV, int C0, int NC>
+static cudaError_t launch_bwd_main(const BwdParams& p, const CUtensorMap* maps, int* ticket,
+                                   int n_work, int prof_id, cudaStream_t st) {
+  using Cfg = BwdCfg<DQK, DV, NC>;
+  auto kern = p.spt ? attn_bwd_main_kernel<DQK, DV, C0, NC, true>
+                    : attn_bwd_main_kernel<DQK, DV, C0, NC, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
-  if (n_work > 0 && D == 128 && p.pairs) {
-    // CTA pairs: n_work pairs of 256 keys
-    int* ticket = p.deterministic ? p.sem + n_sem : nullptr;
-    e = launch_attn_bwd_pair_main(p, maps, n_work, ticket, st);
-    if (e != cudaSuccess) return e;
-  } else if (n_work > 0) {
-    using Cfg = BwdCfg<D>;
-    auto kern = p.spt ? attn_bwd_main_kernel<D, true> : attn_bwd_main_kernel<D, false>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    int* ticket = p.deterministic ? p.sem + n_sem : nullptr;
-    slot = prof_begin(kKBwdMain, st);
-    kern<<<n_work, 512, Cfg::kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p,
-                                               ticket);
-    e = cudaGetLastError();
-    prof_end(slot, st);
-    if (e != cudaSuccess) return e;
-  }
-  const long long n_vec8 = n_rowheads * D / 8;
-  want = (n_vec8 + threads - 1) / threads;
-  blocks = static_cast<int>(want < 152 * 16 ? (want > 0 ? want : 1) : 152 * 16);
-  slot = prof_begin(kKBwdPost, st);
-  attn_bwd_post_kernel<D><<<blocks, threads, 0, st>>>(p, n_vec8);
+  const int slot = prof_begin(prof_id, st);
+  kern<<<n_work, 512, Cfg::kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p, ticket);
   e = cudaGetLastError();
   prof_end(slot, st);
   return e;
 }
 
+// n_sem: ordering semaphores of one pass (deterministic mode); each pass has
+// its own set, followed by its work-ticket counter.
+template <int DQK, int DV>
+static cudaError_t launch_bwd_impl(const BwdParams& p, const CUtensorMap* maps, cudaStream_t st,
+                                   long long rows_q, int n_sem, int n_work) {
+  constexpr int kPasses = DQK > 128 ? 2 : 1;
+  const long long n_rowheads = rows_q * p.H_q;
+  const long long n_acc4 = n_rowheads * DQK / 4;
+  const int threads = 256;
+  long long want = (n_acc4 + threads - 1) / threads;
+  int blocks = static_cast<int>(want < 152 * 16 ? (want > 0 ? want : 1) : 152 * 16);
+  int slot = prof_begin(kKBwdPre, st);
+  attn_bwd_pre_kernel<DV><<<blocks, threads, 0, st>>>(p, n_rowheads, n_acc4,
+                                                      kPasses * (n_sem + 1) - 1);
+  cudaError_t e = cudaGetLastError();
+  prof_end(slot, st);
+  if (e != cudaSuccess) return e;
+  if (n_work > 0 && DQK == 128 && DV == 128 && p.pairs) {
+    // CTA pairs: n_work pairs of 256 keys
+    int* ticket = p.deterministic ? p.sem + n_sem : nullptr;
+    e = launch_attn_bwd_pair_main(p, maps, n_work, ticket, st);
+    if (e != cudaSuccess) return e;
+  } else if (n_work > 0) {
+    int* ticket = p.deterministic ? p.sem + n_sem : nullptr;
+    e = launch_bwd_main<DQK, DV, 0, (DQK < 128 ? DQK : 128)>(p, maps, ticket, n_work, kKBwdMain, st);
+    if (e != cudaSuccess) return e;
+    if constexpr (kPasses == 2) {
+      // query/key head columns 128 .. DQK - 1: S and dP recomputed, dK and dQ
+      // for those columns, no dV
+      BwdParams p1 = p;
+      if (p.deterministic) p1.sem = p.sem + (n_sem + 1);
+      e = launch_bwd_main<DQK, DV, 128, DQK - 128>(p1, maps, p.deterministic ? p1.sem + n_sem : nullptr,
+                                                  n_work, kKBwdMain2, st);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  const long long n_vec8 = n_rowheads * DQK / 8;
+  want = (n_vec8 + threads - 1) / threads;
+  blocks = static_cast<int>(want < 152 * 16 ? (want > 0 ? want : 1) : 152 * 16);
+  slot = prof_begin(kKBwdPost, st);
+  attn_bwd_post_kernel<<<blocks, threads, 0, st>>>(p, n_vec8);
+  e = cudaGetLastError();
+  prof_end(slot, st);
+  return e;
+}
+
+// Supported (d_qk, d_v): (64, 64), (128, 128), (192, 128); the caller checks.
 cudaError_t launch_attn_bwd(const BwdParams& p, const CUtensorMap* maps, cudaStream_t stream,
                             long long rows_q, int n_sem, int n_work) {
-  if (p.d == 64) return launch_bwd_impl<64>(p, maps, stream, rows_q, n_sem, n_work);
-  return launch_bwd_impl<128>(p, maps, stream, rows_q, n_sem, n_work);
+  if (p.d == 64) return launch_bwd_impl<64, 64>(p, maps, stream, rows_q, n_sem, n_work);
+  if (p.d == 192) return launch_bwd_impl<192, 128>(p, maps, stream, rows_q, n_sem, n_work);
+  return launch_bwd_impl<128, 128>(p, maps, stream, rows_q, n_sem, n_work);
 }
 
 }  // namespace attn

@@ -103,21 +103,24 @@ __device__ __forceinline__ bool decode_pair_tile(const BwdParams& p, int idx, ui
     t.Lk = p.N_k;
     t.sem_base = t.b * ((p.N_q + kTileM - 1) / kTileM);
   } else {
+    // sequences in order, each clamped after the one before it (seq_span), so
+    // their query-tile slots stay within the semaphore array
     int s = 0, qslots = 0;
+    SeqSpan sp{0, 0};
     for (; s < p.B; ++s) {
-      const int L = p.cu_seqlens[s + 1] - p.cu_seqlens[s];
-      const int nJ = (L + 2 * kTileN - 1) / (2 * kTileN);
+      sp = seq_span(p.cu_seqlens, s, p.N_q, sp.start + sp.len);
+      const int nJ = (sp.len + 2 * kTileN - 1) / (2 * kTileN);
       if (idx < nJ * p.H_kv) break;
       idx -= nJ * p.H_kv;
-      qslots += (L + kTileM - 1) / kTileM;
+      qslots += (sp.len + kTileM - 1) / kTileM;
     }
     if (s >= p.B) return false;
-    const int L = p.cu_seqlens[s + 1] - p.cu_seqlens[s];
+    const int L = sp.len;
     const int nJ = (L + 2 * kTileN - 1) / (2 * kTileN);
     t.J = idx % nJ;
     t.h_kv = idx / nJ;
     t.b = s;
-    t.row_base = p.cu_seqlens[s];
+    t.row_base = sp.start;
     t.batch_coord = 0;
     t.Lq = L;
     t.Lk = L;

@@ -20,7 +20,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 // 2^8 = 256 (FlashAttention-4 summary, section 3.1.4).
 constexpr float kTau = 8.0f;
 
-enum DevErr : int { kErrNone = 0, kErrTimeout = 1 };
+// Device error word values (the first failure is kept): a bounded wait ran
+// out; a packed-sequence offset array is not 0, non-decreasing, ..., T.
+enum DevErr : int { kErrNone = 0, kErrTimeout = 1, kErrSeqlens = 2 };
 // Host-injected faults (attn_debug_inject); none of them can fault or hang the GPU.
 enum Fault : int { kFaultNone = 0, kFaultSkipDqRelease = 1 };
 
@@ -54,7 +56,8 @@ struct BwdParams {
   float* dvec;          // fp32 D, laid out like lse
   int* sem;             // deterministic mode: one counter per (b, h_q, query tile)
   const int* cu_seqlens;
-  int B, H_q, H_kv, N_q, N_k, group, d;
+  int B, H_q, H_kv, N_q, N_k, group, d;  // d: query/key head dimension
+  int d_v;                               // value head dimension
   int causal, deterministic;
   int n_nblocks;        // key tiles per (batch, kv head) or upper bound (packed)
   int n_mtiles;         // query tiles per (batch, head) (fixed length) or upper bound
@@ -70,7 +73,7 @@ struct BwdParams {
 // Kernel tracing (host side, implemented next to the C ABI). prof_begin
 // returns a slot (or -1 when tracing is off); prof_end closes it.
 enum KernelId : int { kKFwd = 1, kKBwdPre = 2, kKBwdMain = 3, kKBwdPost = 4, kKExp2 = 5,
-                      kKStall = 6, kKFwdPlan = 7, kKFwdPair = 8 };
+                      kKStall = 6, kKFwdPlan = 7, kKFwdPair = 8, kKBwdMain2 = 9 };
 int prof_begin(int kernel, cudaStream_t stream);
 void prof_end(int slot, cudaStream_t stream);
 
@@ -93,6 +96,34 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk16) {
 // Records the first device-side failure; never traps.
 __device__ __forceinline__ void record_error(int* err, int code) {
   if (err != nullptr) atomicCAS(err, 0, code);
+}
+
+// Rows [start, start + len) of packed sequence s, read from cu_seqlens and
+// clamped so that they always lie inside the T packed rows the tensors hold,
+// whatever the array contains: start = clamp(cu[s], lo, T), end =
+// clamp(cu[s + 1], start, T). With lo = 0 each sequence is clamped on its own;
+// a caller that walks the sequences in order passes the previous sequence's
+// end as lo, which also keeps the spans disjoint and their total within T. A
+// valid array (cu[0] = 0, non-decreasing, cu[B] = T) is returned unchanged;
+// check_cu_seqlens reports an invalid one.
+struct SeqSpan {
+  int start, len;
+};
+__device__ __forceinline__ SeqSpan seq_span(const int* cu, int s, int T, int lo) {
+  const int a = min(max(__ldg(cu + s), lo), T);
+  const int e = min(max(__ldg(cu + s + 1), a), T);
+  return SeqSpan{a, e - a};
+}
+
+// Records kErrSeqlens unless cu[0] = 0, cu[s] <= cu[s + 1] and cu[B] = T;
+// thread `tid` of `nthreads` checks its share of the B + 1 entries.
+__device__ __forceinline__ void check_cu_seqlens(const int* cu, int B, int T, int* err,
+                                                 long long tid, long long nthreads) {
+  for (long long s = tid; s <= B; s += nthreads) {
+    const int c = __ldg(cu + s);
+    const bool bad = (s == 0 && c != 0) || (s == B && c != T) || (s < B && c > __ldg(cu + s + 1));
+    if (bad) record_error(err, kErrSeqlens);
+  }
 }
 
 // 2^x on the FMA pipe: Cody-Waite split x = floor(x) + f, f in [0, 1), a

@@ -29,12 +29,29 @@
 // TMEM (512 columns): O_0 [0, d), O_1 [d, 2d), S_0/P_0 [2d, 2d+128),
 // S_1/P_1 [2d+128, 2d+256).
 #include <cstdint>
+#include <type_traits>
 #include <cuda_runtime.h>
 
 #include "attn_common.cuh"
 #include "fwd_softmax.cuh"
 
 namespace attn {
+
+// P can go to the tensor core in two stages (FlashAttention-4 summary, section
+// 3.1.2): the softmax warpgroup stores the first kPWords0 packed words of each
+// row (keys [0, 2 kPWords0)), signals p_part, and the MMA warp starts O += P V
+// on those keys while the rest of the row is exponentiated; p_full covers the
+// remaining words. 48 words = three quarters of the 128 keys = 6 of the 8
+// K-steps of the PV MMA; 64 stores P in one piece. Measured on GB300 the staged
+// store is 2-3% slower on every workload (the extra barrier costs the issuing
+// thread more than an earlier start of PV gains while the other query tile's
+// MMAs keep the tensor core busy), so one piece is the default.
+#ifndef ATTN_FWD_P_WORDS0
+#define ATTN_FWD_P_WORDS0 64
+#endif
+constexpr int kPWords0 = ATTN_FWD_P_WORDS0;
+static_assert(kPWords0 == 48 || kPWords0 == 64, "P split: three quarters or none");
+constexpr int kPvSteps0 = kPWords0 / 8;  // PV K-steps (16 keys each) on the first part
 
 // Shared-memory plan. Q/K rows have DQK columns, V/O rows DV columns; every
 // tile is stored as 128-row x 64-column (16 KB) 128-byte-swizzled blocks.
@@ -88,7 +105,8 @@ struct FwdWork {
 struct FwdBars {
   uint64_t q_full, q_empty;
   uint64_t s_full[2];
-  uint64_t p_full[2];
+  uint64_t p_part[2];   // the first kPWords0 packed P words of the row are in TMEM
+  uint64_t p_full[2];   // all of P is in TMEM
   uint64_t pv_done[2];
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
@@ -120,8 +138,9 @@ __device__ __forceinline__ FwdWork locate_fwd_work(const FwdParams& p, int v) {
     }
     w.b = p.seq_order[lo];
     w.local = v - p.tile_start[lo];
-    w.row_base = p.cu_seqlens[w.b];
-    w.L = p.cu_seqlens[w.b + 1] - w.row_base;
+    const SeqSpan sp = seq_span(p.cu_seqlens, w.b, p.N_q, 0);
+    w.row_base = sp.start;
+    w.L = sp.len;
   }
   return w;
 }
@@ -201,6 +220,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     mbar_init(smem_addr(&bars->q_empty), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&bars->s_full[i]), 1);
+      mbar_init(smem_addr(&bars->p_part[i]), 128);
       mbar_init(smem_addr(&bars->p_full[i]), 128);
       mbar_init(smem_addr(&bars->pv_done[i]), 1);
     }
@@ -379,7 +399,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         mma_commit(smem_addr(&bars->s_full[i]));
       };
-      auto issue_pv = [&](int i, int it, bool acc) {
+      // O_i += P_i V_j over the K-steps [K0, K1) (16 keys each)
+      auto issue_pv = [&](int i, int it, bool acc, auto k0_, auto k1_) {
+        constexpr int K0 = decltype(k0_)::value, K1 = decltype(k1_)::value;
         uint64_t vb;
         if constexpr (Cfg::kBlockRing) {
           const uint32_t slot = pos_of(it) % Cfg::kSlots;
@@ -390,9 +412,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t d_tmem = tmem + Cfg::kColO0 + i * DV;
         const uint32_t a_tmem = tmem + Cfg::kColS0 + i * 128;
 #pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)
+        for (int kk = K0; kk < K1; ++kk)
           mma_ts(d_tmem, a_tmem + kk * 8, vb + kk * (2048 >> 4), kIdPV, (acc || kk > 0));
       };
+      using KAll0 = std::integral_constant<int, 0>;
+      using KPart = std::integral_constant<int, kPvSteps0>;
+      using KAll1 = std::integral_constant<int, kTileN / 16>;
       int pw[2] = {0, 0};  // p_full waits so far, per query tile
       int qk = 0;          // tiles with a Q load
       bool ok = true;
@@ -425,10 +450,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             if (j >= t.n[i]) continue;
-            if (!mbar_wait(smem_addr(&bars->p_full[i]), pw[i] & 1, lim)) { ok = false; break; }
+            if constexpr (kPvSteps0 < kTileN / 16) {
+              // the first three quarters of P_i, then the rest
+              if (!mbar_wait(smem_addr(&bars->p_part[i]), pw[i] & 1, lim)) { ok = false; break; }
+              tc_fence_after();
+              issue_pv(i, itv, j > 0, KAll0{}, KPart{});
+              if (!mbar_wait(smem_addr(&bars->p_full[i]), pw[i] & 1, lim)) { ok = false; break; }
+              tc_fence_after();
+              issue_pv(i, itv, true, KPart{}, KAll1{});
+            } else {
+              if (!mbar_wait(smem_addr(&bars->p_full[i]), pw[i] & 1, lim)) { ok = false; break; }
+              tc_fence_after();
+              issue_pv(i, itv, j > 0, KAll0{}, KAll1{});
+            }
             ++pw[i];
-            tc_fence_after();
-            issue_pv(i, itv, j > 0);
             if constexpr (Cfg::kBlockRing) {
               if (i == 1 || j >= t.n[1]) release(itv);  // the last PV reading V_j
             }
@@ -495,15 +530,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         uint32_t pk[64];
         bool rescale_warp;
         float factor;
-        if (c > 0.0f)
-          softmax_row_tile<EMU, true>(s, c, m_used, l, kv0, qrow, Lk, need_mask, p.causal, pk,
+        const bool pos = c > 0.0f;
+        const float mb =
+            pos ? softmax_row_max<true>(s, c, m_used, l, kv0, qrow, Lk, need_mask, p.causal,
+                                        rescale_warp, factor)
+                : softmax_row_max<false>(s, c, m_used, l, kv0, qrow, Lk, need_mask, p.causal,
                                          rescale_warp, factor);
-        else
-          softmax_row_tile<0, false>(s, c, m_used, l, kv0, qrow, Lk, need_mask, p.causal, pk,
-                                        rescale_warp, factor);
+        uint64_t sum2[2] = {0ull, 0ull};
+        if (pos) softmax_row_exp<EMU, true, 0, kPWords0>(s, c, mb, need_mask, pk, sum2);
+        else softmax_row_exp<0, false, 0, kPWords0>(s, c, mb, need_mask, pk, sum2);
         if (rescale_warp && j > 0 && __any_sync(0xffffffffu, factor != 1.0f)) {
           // correction: O_{j-1} is complete here, because the commit that
-          // signalled S_j came from the thread that issued PV_{j-1} before S_j
+          // signalled S_j came from the thread that issued PV_{j-1} before S_j;
+          // it is back in TMEM before the first part of P is signalled, so
+          // before PV_j adds to O
 #pragma unroll
           for (int cc = 0; cc < DV / 32; ++cc) {
             uint32_t ov[32];
@@ -515,10 +555,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         }
         tmem_st32(tmem + lane_base + col_s, *reinterpret_cast<uint32_t(*)[32]>(pk));
-        tmem_st32(tmem + lane_base + col_s + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+        if constexpr (kPWords0 < 64) {
+          tmem_st16(tmem + lane_base + col_s + 32, *reinterpret_cast<uint32_t(*)[16]>(pk + 32));
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(smem_addr(&bars->p_part[i]));
+          if (pos) softmax_row_exp<EMU, true, kPWords0, 64>(s, c, mb, need_mask, pk, sum2);
+          else softmax_row_exp<0, false, kPWords0, 64>(s, c, mb, need_mask, pk, sum2);
+          tmem_st16(tmem + lane_base + col_s + 48, *reinterpret_cast<uint32_t(*)[16]>(pk + 48));
+        } else {
+          tmem_st32(tmem + lane_base + col_s + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_addr(&bars->p_full[i]));
+        l += softmax_row_sum(sum2);
       }
       if (!ok) break;
       // -------------------------------------------------------- epilogue
@@ -586,15 +637,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // varlen scheduling paragraph). One CTA. Ties keep their input order; with
 // sort == 0 the input order is kept.
 __global__ void __launch_bounds__(1024)
-fwd_plan_kernel(const int* __restrict__ cu_seqlens, int B, int H_q, int pair_heads, int sort,
-                int* seq_order, int* tile_start) {
+fwd_plan_kernel(const int* __restrict__ cu_seqlens, int B, int T, int H_q, int pair_heads, int sort,
+                int* seq_order, int* tile_start, int* err) {
   extern __shared__ int plan_smem[];
   int* len = plan_smem;        // [B] when sorting
   int* ord = plan_smem + B;    // [B] when sorting
   __shared__ int warp_sum[32];
   const int tid = threadIdx.x;
+  // the lengths are those the forward decodes (clamped into the T packed rows);
+  // an inconsistent offset array is reported through the error word
+  check_cu_seqlens(cu_seqlens, B, T, err, tid, blockDim.x);
   if (sort) {
-    for (int s = tid; s < B; s += blockDim.x) len[s] = cu_seqlens[s + 1] - cu_seqlens[s];
+    for (int s = tid; s < B; s += blockDim.x) len[s] = seq_span(cu_seqlens, s, T, 0).len;
     __syncthreads();
     for (int s = tid; s < B; s += blockDim.x) {
       const int L = len[s];
@@ -613,7 +667,7 @@ fwd_plan_kernel(const int* __restrict__ cu_seqlens, int B, int H_q, int pair_hea
   const int v0 = min(B, tid * chunk), v1 = min(B, v0 + chunk);
   auto tiles_of = [&](int vs) {
     const int s = sort ? ord[vs] : vs;
-    const int L = sort ? len[s] : (cu_seqlens[s + 1] - cu_seqlens[s]);
+    const int L = sort ? len[s] : seq_span(cu_seqlens, s, T, 0).len;
     const int mrows = (2 * kTileM) >> pair_heads;
     return (L + mrows - 1) / mrows * (H_q >> pair_heads);
   };
@@ -686,16 +740,16 @@ cudaError_t launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUte
 // shared memory); larger batches keep their input order.
 constexpr int kPlanMaxSort = 8192;
 
-cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int H_q, int pair_heads, int* seq_order,
-                            int* tile_start, cudaStream_t stream) {
+cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int T, int H_q, int pair_heads,
+                            int* seq_order, int* tile_start, int* err, cudaStream_t stream) {
   const int sort = (B <= kPlanMaxSort) ? 1 : 0;
   const size_t smem = sort ? static_cast<size_t>(2) * B * sizeof(int) : 0;
   cudaError_t e = cudaFuncSetAttribute(fwd_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        2 * kPlanMaxSort * static_cast<int>(sizeof(int)));
   if (e != cudaSuccess) return e;
   const int slot = prof_begin(kKFwdPlan, stream);
-  fwd_plan_kernel<<<1, 1024, smem, stream>>>(cu_seqlens, B, H_q, pair_heads, sort, seq_order,
-                                              tile_start);
+  fwd_plan_kernel<<<1, 1024, smem, stream>>>(cu_seqlens, B, T, H_q, pair_heads, sort, seq_order,
+                                              tile_start, err);
   e = cudaGetLastError();
   prof_end(slot, stream);
   return e;

@@ -89,9 +89,12 @@ __device__ __forceinline__ bool decode_pair_fwd_tile(const FwdParams& p, uint32_
     t.Lq = p.N_q;
     t.Lk = p.N_k;
   } else {
+    // sequences in order, each clamped after the one before it (seq_span)
     int idx = pidx, s = 0, L = 0, nb = 0;
+    SeqSpan sp{0, 0};
     for (; s < p.B; ++s) {
-      L = p.cu_seqlens[s + 1] - p.cu_seqlens[s];
+      sp = seq_span(p.cu_seqlens, s, p.N_q, sp.start + sp.len);
+      L = sp.len;
       nb = (L + R - 1) / R;
       if (idx < nb) break;
       idx -= nb;
@@ -99,7 +102,7 @@ __device__ __forceinline__ bool decode_pair_fwd_tile(const FwdParams& p, uint32_
     if (s >= p.B) return false;
     m = p.causal ? (nb - 1 - idx) : idx;
     t.b = s;
-    t.row_base = p.cu_seqlens[s];
+    t.row_base = sp.start;
     t.batch_coord = 0;
     t.Lq = L;
     t.Lk = L;
@@ -172,6 +175,10 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
   PairFwdBars* bars = reinterpret_cast<PairFwdBars*>(smem + Cfg::kBarOff);
   const uint32_t rank = cluster_ctarank();
 
+  // the first CTA reports an inconsistent packed-sequence offset array (every
+  // CTA clamps what it decodes, so it stays inside the tensors either way)
+  if (p.cu_seqlens != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+    check_cu_seqlens(p.cu_seqlens, p.B, p.N_q, p.err, threadIdx.x, blockDim.x);
   PairFwdTile t;
   if (!decode_pair_fwd_tile(p, rank, t)) return;  // both CTAs of the pair leave together
 

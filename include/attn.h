@@ -59,6 +59,20 @@
  * failure returns ATTN_ERR_CUDA. Device-side pipeline waits are bounded: if one
  * ever runs out of time the kernel records ATTN_ERR_TIMEOUT in the device error
  * word and returns; attn_check() reports (and clears) it.
+ *
+ * Packed offsets are device data the host does not read. The kernels clamp every
+ * sequence they decode into the T = N_q packed rows (rows
+ * [clamp(cu[s], lo, T), clamp(cu[s+1], start, T)), lo = 0 or the previous
+ * sequence's end), so no read or write leaves the caller's buffers whatever the
+ * array holds. An array that is not 0, non-decreasing, ..., T is reported as
+ * ATTN_ERR_SEQLENS through the device error word (attn_check); the results of
+ * such a call are undefined, and rows that no clamped sequence covers are not
+ * written.
+ *
+ * Device resets. The library caches per-device state (the error word's address,
+ * the plan buffers and balanced lists above). Calls made after cudaDeviceReset
+ * (or any other teardown of the device's primary context) in the same process
+ * are unsupported.
  */
 #ifndef ATTN_H_
 #define ATTN_H_
@@ -83,7 +97,8 @@ typedef enum {
   ATTN_ERR_CUDA = 8,                 /* a CUDA runtime call or launch failed */
   ATTN_ERR_TIMEOUT = 9,              /* a device-side bounded wait ran out */
   ATTN_ERR_NO_DEVICE = 10,           /* no usable CUDA device */
-  ATTN_ERR_UNSUPPORTED_DEVICE = 11   /* device is not sm_103 (GB300-class) */
+  ATTN_ERR_UNSUPPORTED_DEVICE = 11,  /* device is not sm_103 (GB300-class) */
+  ATTN_ERR_SEQLENS = 12              /* cu_seqlens is not 0, non-decreasing, ..., N_q */
 } attn_status;
 
 /*
@@ -124,8 +139,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * in q and k and by d_v in v and o: q [B, N_q, H_q, d_qk], k [B, N_k, H_kv, d_qk],
  * v [B, N_k, H_kv, d_v], o [B, N_q, H_q, d_v] (packed: [T, H, d_*]). Everything
  * else (lse, masks, packed inputs, errors, ownership, streams) is as for
- * attn_fwd, which is this call with d_qk = d_v = d. attn_bwd supports only
- * equal head dimensions.
+ * attn_fwd, which is this call with d_qk = d_v = d. attn_bwd_dims is the
+ * matching backward pass.
  */
 int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* lse,
                   int B, int H_q, int H_kv, int N_q, int N_k, int d_qk, int d_v, int causal,
@@ -168,6 +183,31 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              void* workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * Backward pass with separate head dimensions for queries/keys (d_qk) and for
+ * values/outputs (d_v), the gradient of attn_fwd_dims: layouts as there, with
+ * dq like q [.., H_q, d_qk], dk like k [.., H_kv, d_qk], dv like v
+ * [.., H_kv, d_v], o and dout [.., H_q, d_v]. Supported pairs: (64, 64),
+ * (128, 128), (192, 128); anything else returns ATTN_ERR_UNSUPPORTED_HEADDIM.
+ * attn_bwd is this call with d_qk = d_v = d. The FlashAttention-4 summary
+ * (experimental setup) benchmarks the (192, 128) head dimensions of the
+ * DeepSeek V3 architecture.
+ *
+ * At d_qk = 192 the main kernel runs in two passes over the key tiles: the
+ * first accumulates dV and the query/key head columns 0-127 of dK and dQ, the
+ * second columns 128-191; both recompute S and dP (the tensor memory of one
+ * SM holds dV, dK, S and dP/dQ for 128 columns, not 192). Everything else
+ * (workspace, determinism, errors, streams) is as for attn_bwd, with the
+ * workspace size from attn_bwd_dims_workspace_bytes.
+ */
+size_t attn_bwd_dims_workspace_bytes(int B, int H_q, int H_kv, int N_q, int N_k, int d_qk,
+                                     int d_v, int varlen, int deterministic);
+int attn_bwd_dims(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv,
+                  int B, int H_q, int H_kv, int N_q, int N_k, int d_qk, int d_v, int causal,
+                  const int* seqlens, float scale, int deterministic,
+                  void* workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
  * Size of the library's own scratch buffer used by attn_bwd_noalloc: 64 MiB on
  * every GPU that loads the library, held until the process exits.
  */
@@ -185,9 +225,10 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
  * outputs are still caller-owned. The scratch is a fixed
  * ATTN_NOALLOC_SCRATCH_BYTES buffer inside the library's device code; nothing is
  * allocated. Problems whose attn_bwd_workspace_bytes(...) exceeds that size are
- * rejected with ATTN_ERR_WORKSPACE before anything is launched. The first call on
- * a device looks up the buffer's device address for that device (with the
- * device current); make that first call before any stream capture. All calls on
+ * rejected with ATTN_ERR_WORKSPACE before anything is launched. Every call looks
+ * up the buffer's device address on the current device (a lookup, no
+ * allocation); the first lookup on a device loads the library's device code
+ * there, so make the first call on a device before any stream capture. All calls on
  * a device share the one buffer and it keeps the last call's contents (the call
  * clears what must start at zero), so calls whose kernels overlap on the GPU
  * (different streams, or different host threads) race on it and give wrong
@@ -199,10 +240,11 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                      const int* seqlens, float scale, int deterministic, attn_stream_t stream);
 
 /*
- * Synchronises `stream`, then returns ATTN_ERR_TIMEOUT if a kernel of this
- * library on the current device recorded a timed-out wait since the last check
- * (and clears the record), ATTN_ERR_CUDA if the stream reports an error, else
- * ATTN_OK.
+ * Synchronises `stream`, then returns the first failure a kernel of this library
+ * on the current device recorded since the last check (and clears the record):
+ * ATTN_ERR_TIMEOUT for a timed-out wait, ATTN_ERR_SEQLENS for an inconsistent
+ * packed-sequence offset array; ATTN_ERR_CUDA if the stream reports an error;
+ * else ATTN_OK.
  */
 int attn_check(attn_stream_t stream);
 
@@ -313,9 +355,10 @@ long long attn_set_wait_limit(long long cycles);
  * attn_profile_read() waits for the recorded events, copies up to
  * `max_records` records (oldest first) and discards everything it has read;
  * it returns the number of records written, or a negative attn_status.
- * Kernel ids: 1 forward, 2 backward pre (D, zeroing), 3 backward main,
- * 4 backward post (dQ conversion), 5 exp2 test hook, 6 stall test hook, 7 forward
- * planning kernel (packed inputs), 8 forward on CTA pairs (ATTN_FWD_CTA_PAIR).
+ * Kernel ids: 1 forward, 2 backward pre (D, zeroing), 3 backward main (its first
+ * pass at d_qk = 192), 4 backward post (dQ conversion), 5 exp2 test hook, 6 stall
+ * test hook, 7 forward planning kernel (packed inputs), 8 forward on CTA pairs
+ * (ATTN_FWD_CTA_PAIR), 9 second pass of the backward main kernel (d_qk = 192).
  */
 typedef struct {
   int kernel;  /* kernel id, see above */

@@ -36,9 +36,9 @@ def test_forward_rejects_host_or_wrong_dtype():
     _raises("contiguous bf16 CUDA", binding.forward, f, f, f)
 
 
-def test_backward_needs_equal_head_dims_and_matching_tensors():
-    q, k, v = _t(1, 8, 2, 192), _t(1, 8, 2, 192), _t(1, 8, 2, 128)
-    _raises("equal query/key and value head dimensions", binding.backward, q, k, v, None, None, None)
+def test_backward_checks_head_dims_and_matching_tensors():
+    q, k, v = _t(1, 8, 2, 192), _t(1, 8, 2, 128), _t(1, 8, 2, 128)
+    _raises("q and k head dimensions differ", binding.backward, q, k, v, None, None, None)
     q = _t(1, 8, 2, 64)
     _raises("contiguous bf16 CUDA", binding.backward, q, q, q, q, _t(1, 2, 8, dtype=torch.float32), q)
 
@@ -54,3 +54,7 @@ def test_forward_checks_out_and_lse_before_launch(monkeypatch):
     _raises("o must be", binding.backward, q, q, q, _t(1, 8, 2, 32), _t(1, 2, 8, dtype=torch.float32), q)
     _raises("dout must be", binding.backward, q, q, q, q, _t(1, 2, 8, dtype=torch.float32), _t(1, 8, 1, 64))
     _raises("lse must be", binding.backward, q, q, q, q, _t(1, 2, 9, dtype=torch.float32), q)
+    # separate head dimensions: o and dout have v's width
+    q1, v1 = _t(1, 8, 2, 192), _t(1, 8, 2, 128)
+    _raises("o must be", binding.backward, q1, q1, v1, q1, _t(1, 2, 8, dtype=torch.float32), v1)
+    _raises("dout must be", binding.backward, q1, q1, v1, v1, _t(1, 2, 8, dtype=torch.float32), q1)

@@ -140,8 +140,9 @@ def test_worked_example_on_gpu(d):
         assert abs(float(lse.cpu()[0, 0, 0]) - ref_lse) < 2e-3
 
 
-# d_qk = 192, d_v = 128 (forward only). Eight or more key tiles put a V tile
-# across the end of the block ring (its column blocks in slots 7 and 0).
+# d_qk = 192, d_v = 128. Eight or more key tiles put a V tile across the end of
+# the forward's block ring (its column blocks in slots 7 and 0); the backward
+# runs its two passes (query/key head columns 0-127 with dV, then 128-191).
 ASYM = {
     "asym_ragged_causal": dict(B=2, H_q=2, H_kv=2, N_q=300, N_k=300, causal=True),
     "asym_gqa_ring_wrap": dict(B=1, H_q=4, H_kv=2, N_q=1000, N_k=1000, causal=False),
@@ -159,6 +160,16 @@ def test_asymmetric_head_dims_forward(name):
     o, lse, _ = run_forward(inp)
     assert tuple(o.shape[-1:]) == (128,)
     _oracle_fwd_check(inp, o, lse, _all_pairs(inp))
+
+
+@pytest.mark.parametrize("name", list(ASYM))
+def test_asymmetric_head_dims_backward(name):
+    inp = W.custom(seed=200 + len(name), d=192, d_v=128, **ASYM[name])
+    o, lse, dev = run_forward(inp)
+    dq, dk, dv = run_backward(inp, o, lse, dev)
+    assert tuple(dq.shape[-1:]) == (192,) and tuple(dk.shape[-1:]) == (192,)
+    assert tuple(dv.shape[-1:]) == (128,)
+    _oracle_bwd_check(inp, dq, dk, dv, _all_groups(inp))
 
 
 @pytest.mark.parametrize("B,H,N,d,H_kv", [(2, 16, 8192, 64, 16), (1, 16, 8192, 128, 16),
@@ -329,7 +340,7 @@ def test_workload_forward(name, n_pairs, n_rows):
 
 
 BWD_FULL = [("tiny", None), ("short", 3), ("short_causal", 3), ("mid", 1), ("mid_causal", 1),
-            ("long", 1), ("varlen_gqa", 1)]
+            ("long", 1), ("varlen_gqa", 1), ("mla", 1), ("mla_causal", 1)]
 
 
 @pytest.mark.parametrize("name,n_groups", BWD_FULL, ids=[f[0] for f in BWD_FULL])
@@ -351,6 +362,10 @@ DET_CUSTOM = {
     "spt_ragged": dict(B=1, H_q=4, H_kv=1, N_q=1100, N_k=1100, d=128, causal=True),
     # different query and key lengths: ascending key-tile order
     "ascending_cross": dict(B=2, H_q=2, H_kv=2, N_q=300, N_k=700, d=64, causal=False),
+    # separate head dimensions: each of the two passes has its own ordering
+    "asym_spt": dict(B=1, H_q=4, H_kv=2, N_q=1100, N_k=1100, d=192, d_v=128, causal=True),
+    "asym_rotated_packed": dict(B=0, H_q=2, H_kv=1, N_q=0, N_k=0, d=192, d_v=128, causal=False,
+                                seqlens=[300, 700, 129]),
 }
 
 
