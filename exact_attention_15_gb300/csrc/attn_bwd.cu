@@ -231,24 +231,6 @@ __global__ void __launch_bounds__(256) attn_bwd_post_kernel(const BwdParams p, l
 
 
 
-// dQ of a pass with 128 query/key head columns is computed transposed, dQ^T =
-// K^T dS^T (the same two shared-memory operands as dS K, A and B swapped), so
-// that TMEM lane = head column and column = query: after a 32x32b TMEM load a
-// warp holds 32 consecutive head columns of each query row, and every
-// red.global.add.f32 warp instruction covers one whole 128-byte line of the dQ
-// accumulator. That replaces the shared-memory staging of dQ (a 64 KB write
-// and a 64 KB read per query tile) in a kernel whose time is set by its
-// shared-memory traffic. Passes of 64 columns (d = 64, and the second pass at
-// d_qk = 192) would need an M = 64 MMA there and keep the staged bulk
-// reductions.
-#ifndef ATTN_BWD_DQ_T
-#define ATTN_BWD_DQ_T 0
-#endif
-
-__device__ __forceinline__ void red_add_f32(float* addr, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
-}
-
 template <int DQK, int DV, int C0, int NC, bool SPT>
 __global__ void __launch_bounds__(512, 1)
 attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -257,7 +239,6 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
   using Cfg = BwdCfg<DQK, DV, NC>;
   constexpr bool kDoDV = C0 == 0;          // this pass also accumulates dV
   constexpr int kQS = Cfg::kQStages;
-  constexpr bool kDqT = ATTN_BWD_DQ_T && NC == 128;  // dQ^T in TMEM, reduced from registers
   extern __shared__ __align__(1024) uint8_t smem[];
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + Cfg::kBarOff);
 
@@ -386,12 +367,14 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       // reader of Q_i, is done:
       //   S_0, dP_0 | dV_i, dK_i, dQ_i, S_{i+1}, dP_{i+1} | ...
       // A pass without dV skips it; dK and dQ cover the pass's NC columns.
-      if (lane == 0 && n_it > 0) {
+      // The whole warp runs the issue loop (warp-uniform descriptors and
+      // phases); one elected lane issues each MMA and commit.
+      if (n_it > 0) {
+        const bool leader = elect_one_sync();
         constexpr uint32_t kIdSS = make_idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
         constexpr uint32_t kIdDV = make_idesc_bf16(128, DV, 0, 1);   // dV: B MN-major
         constexpr uint32_t kIdDK = make_idesc_bf16(128, NC, 0, 1);   // dK: B MN-major
         constexpr uint32_t kIdDQ = make_idesc_bf16(128, NC, 1, 1);   // dQ: A and B MN-major
-        constexpr uint32_t kIdDQT = make_idesc_bf16(NC, 128, 1, 1);  // dQ^T: A and B MN-major
         // Descriptors are built once; each MMA only adds a compile-time byte
         // offset (>> 4) to the start-address field, which keeps the single
         // issuing thread ahead of the tensor core. Every tile is made of
@@ -417,24 +400,24 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           const uint64_t qb = q_km + (it % kQS) * kStageStep;
 #pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk)
-            mma_ss(tmem + Cfg::kColS, k_km + koff(kk), qb + koff(kk), kIdSS, kk > 0);
-          mma_commit(smem_addr(&bars->s_full));
+            mma_ss_by(leader, tmem + Cfg::kColS, k_km + koff(kk), qb + koff(kk), kIdSS, kk > 0);
+          mma_commit_by(leader, smem_addr(&bars->s_full));
         };
         auto issue_dp = [&](int) {  // dP^T = V dO^T
 #pragma unroll
           for (int kk = 0; kk < DV / 16; ++kk)
-            mma_ss(tmem + Cfg::kColDP, v_km + koff(kk), do_km + koff(kk), kIdSS, kk > 0);
-          mma_commit(smem_addr(&bars->dp_full));
+            mma_ss_by(leader, tmem + Cfg::kColDP, v_km + koff(kk), do_km + koff(kk), kIdSS, kk > 0);
+          mma_commit_by(leader, smem_addr(&bars->dp_full));
         };
         auto wait_issue_s = [&](int it) {  // S^T of tile `it` once its Q is in
-          if (!mbar_wait(smem_addr(&bars->q_full[it % kQS]), (it / kQS) & 1, lim)) return false;
+          if (!mbar_wait_warp(smem_addr(&bars->q_full[it % kQS]), (it / kQS) & 1, lim)) return false;
           tc_fence_after();
           issue_s(it);
           return true;
         };
-        bool ok = mbar_wait(smem_addr(&bars->kv_full), 0, lim);
+        bool ok = mbar_wait_warp(smem_addr(&bars->kv_full), 0, lim);
         if (ok) ok = wait_issue_s(0);
-        if (ok) ok = mbar_wait(smem_addr(&bars->do_full), 0, lim);
+        if (ok) ok = mbar_wait_warp(smem_addr(&bars->do_full), 0, lim);
         if (ok) {
           tc_fence_after();
           issue_dp(0);
@@ -442,55 +425,46 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         for (int it = 0; ok && it < n_it; ++it) {
           const int stage = it % kQS;
           // dV += P^T dO  (P^T from TMEM)
-          if (!(ok = mbar_wait(smem_addr(&bars->p_ready), it & 1, lim))) break;
+          if (!(ok = mbar_wait_warp(smem_addr(&bars->p_ready), it & 1, lim))) break;
           tc_fence_after();
           if constexpr (kDoDV) {
             // P^T for queries [0, 64) sits in S^T columns [0, 32), for queries
             // [64, 128) in columns [64, 96); each MMA reads one 16-query slice
 #pragma unroll
             for (int kk = 0; kk < kTileM / 16; ++kk)
-              mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
+              mma_ts_by(leader, tmem + Cfg::kColDV, tmem + Cfg::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
                      do_mn + kk * (2048 >> 4), kIdDV, (it > 0 || kk > 0));
           }
-          mma_commit(smem_addr(&bars->do_empty));  // dO_i fully read: the next one may load
+          mma_commit_by(leader, smem_addr(&bars->do_empty));  // dO_i fully read: the next one may load
           // S^T of the next query tile into the same TMEM columns (the MMAs run
           // in issue order, so dV has read P^T before they are overwritten)
           if (kQS == 2 && it + 1 < n_it && !(ok = wait_issue_s(it + 1))) break;
           // dK += dS^T Q (dS^T: the shared-memory dS buffer read K-major);
           // dQ = dS K (the same buffer read MN-major)
-          if (!(ok = mbar_wait(smem_addr(&bars->ds_ready), it & 1, lim))) break;
+          if (!(ok = mbar_wait_warp(smem_addr(&bars->ds_ready), it & 1, lim))) break;
           tc_fence_after();
           const uint64_t qmn = q_mn + stage * kStageStep;
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk)
-            mma_ss(tmem + Cfg::kColDK, ds_km + koff(kk), qmn + kk * (2048 >> 4), kIdDK,
+            mma_ss_by(leader, tmem + Cfg::kColDK, ds_km + koff(kk), qmn + kk * (2048 >> 4), kIdDK,
                    (it > 0 || kk > 0));
-          if constexpr (kQS == 1) mma_commit(smem_addr(&bars->q_empty[0]));  // Q_i fully read
-          if constexpr (kDqT) {
-            // dQ^T = K^T dS^T: A = the pass's K columns (MN-major, M = head
-            // columns), B = dS (MN-major, N = queries), K-steps over keys
+          if constexpr (kQS == 1) mma_commit_by(leader, smem_addr(&bars->q_empty[0]));  // Q_i fully read
 #pragma unroll
-            for (int kk = 0; kk < kTileN / 16; ++kk)
-              mma_ss(tmem + Cfg::kColDP, k_mn + kk * (2048 >> 4), ds_mn + kk * (2048 >> 4), kIdDQT,
-                     kk > 0);
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < kTileN / 16; ++kk)
-              mma_ss(tmem + Cfg::kColDP, ds_mn + kk * (2048 >> 4), k_mn + kk * (2048 >> 4), kIdDQ,
-                     kk > 0);
-          }
-          mma_commit(smem_addr(&bars->dq_full));  // covers every earlier MMA, dV included
-          if constexpr (kQS == 2) mma_commit(smem_addr(&bars->q_empty[stage]));
+          for (int kk = 0; kk < kTileN / 16; ++kk)
+            mma_ss_by(leader, tmem + Cfg::kColDP, ds_mn + kk * (2048 >> 4), k_mn + kk * (2048 >> 4),
+                      kIdDQ, kk > 0);
+          mma_commit_by(leader, smem_addr(&bars->dq_full));  // covers every earlier MMA, dV included
+          if constexpr (kQS == 2) mma_commit_by(leader, smem_addr(&bars->q_empty[stage]));
           if (kQS == 1 && it + 1 < n_it && !(ok = wait_issue_s(it + 1))) break;
           // dP^T of the next tile reuses the dQ columns once dQ_i has been read out
           if (it + 1 < n_it) {
-            if (!(ok = mbar_wait(smem_addr(&bars->dq_free), it & 1, lim))) break;
-            if (!(ok = mbar_wait(smem_addr(&bars->do_full), (it + 1) & 1, lim))) break;
+            if (!(ok = mbar_wait_warp(smem_addr(&bars->dq_free), it & 1, lim))) break;
+            if (!(ok = mbar_wait_warp(smem_addr(&bars->do_full), (it + 1) & 1, lim))) break;
             tc_fence_after();
             issue_dp(it + 1);
           }
         }
-        if (!ok) record_error(p.err, kErrTimeout);
+        if (!ok && leader) record_error(p.err, kErrTimeout);
       }
     }
     __syncwarp();
@@ -630,9 +604,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
   } else {
     regs_inc<144>();
-    // --------------------------------------------------------- dQ
-    // thread r: query row r of the dQ_i tile, or head column C0 + r of the
-    // transposed tile (kDqT)
+    // --------------------------------------------------------- dQ (query row r)
     const int r = tid - 384;
     const uint32_t lane_base = static_cast<uint32_t>(r & ~31) << 16;
     bool ok = true;
@@ -663,19 +635,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
         named_bar_sync(1, 128);
       }
-      if constexpr (kDqT) {
-        // v[q] = dQ_i[q][C0 + r]: for each query row the warp adds 32
-        // consecutive floats (one 128-byte line); rows past the end of the
-        // sequence or batch entry are skipped (warp-uniform)
-        const int n_rows = min(kTileM, t.Lq - i * kTileM);
-        const size_t row0 = p.cu_seqlens ? static_cast<size_t>(t.row_base) + i * kTileM
-                                         : static_cast<size_t>(t.b) * p.N_q + i * kTileM;
-        float* dst = p.dq_acc + (row0 * p.H_q + h) * DQK + C0 + r;
-        const size_t row_step = static_cast<size_t>(p.H_q) * DQK;
-#pragma unroll
-        for (int q = 0; q < kTileM; ++q)
-          if (q < n_rows) red_add_f32(dst + q * row_step, __uint_as_float(v[q]));
-      } else if (p.cu_seqlens != nullptr && (i + 1) * kTileM > t.Lq) {
+      if (p.cu_seqlens != nullptr && (i + 1) * kTileM > t.Lq) {
         // last tile of a packed sequence: a 128-row bulk reduction would also
         // touch the next sequence's rows, so add the valid rows one by one
         const int q = i * kTileM + r;
@@ -711,7 +671,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
       }
       if (p.deterministic) {
-        if (!kDqT && r == 0) {
+        if (r == 0) {
           bulk_wait_group<0>();  // our reductions are complete in global memory
           fence_async_global();
         }
@@ -723,7 +683,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (r == 0 && !skip) atomicAdd(sem, 1);
       }
     }
-    if (!kDqT && r == 0) bulk_wait_group<0>();  // staging buffers are read before the CTA exits
+    if (r == 0) bulk_wait_group<0>();  // staging buffers are read before the CTA exits
     if (!ok) record_error(p.err, kErrTimeout);
   }
   tc_fence_before();

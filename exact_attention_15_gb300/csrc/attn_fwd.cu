@@ -328,12 +328,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    // One thread issues every MMA. Its issue order alternates the two query
-    // tiles (PV_0, S_0, PV_1, S_1, ...), which keeps the two softmax warpgroups
-    // half an iteration apart, so each one's softmax overlaps the other tile's
-    // MMAs. A tcgen05.mma holds the issuing thread for about its own execution
-    // time, so this thread does as little else as possible between MMAs.
-    if (lane == 0) {
+    // The whole warp runs the issue loop (so descriptors, phases and tile
+    // fields are warp-uniform values) and one elected lane issues each MMA and
+    // commit. The issue order alternates the two query tiles (PV_0, S_0, PV_1,
+    // S_1, ...), which keeps the two softmax warpgroups half an iteration apart,
+    // so each one's softmax overlaps the other tile's MMAs. A tcgen05.mma holds
+    // the issuing lane for about its own execution time, so the loop does as
+    // little else as possible between MMAs.
+    {
+      const bool leader = elect_one_sync();
       constexpr uint32_t kIdS = make_idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t kIdPV = make_idesc_bf16(128, DV, 0, 1);
       constexpr int kQB = Cfg::kQBlocks, kVB = Cfg::kVBlocks;
@@ -365,9 +368,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if constexpr (Cfg::kBlockRing) {
           const uint32_t p0 = pos_of(it);
           const int nb = (it & 1) ? kVB : kQB;
-          for (int b = 0; b < nb; ++b) mma_commit(smem_addr(&bars->kv_empty[(p0 + b) % Cfg::kSlots]));
+          for (int b = 0; b < nb; ++b) mma_commit_by(leader, smem_addr(&bars->kv_empty[(p0 + b) % Cfg::kSlots]));
         } else {
-          mma_commit(smem_addr(&bars->kv_empty[stage_of(it)]));
+          mma_commit_by(leader, smem_addr(&bars->kv_empty[stage_of(it)]));
         }
       };
       auto issue_s = [&](int i, int it) {
@@ -386,7 +389,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int k4 = 0; k4 < 4; ++k4) {
               const int kk = 4 * b + k4;
               const uint32_t qoff = (b * 16384 + k4 * 32) >> 4;
-              mma_ss(d_tmem, qa + qoff, kb + ((k4 * 32) >> 4), kIdS, kk > 0);
+              mma_ss_by(leader, d_tmem, qa + qoff, kb + ((k4 * 32) >> 4), kIdS, kk > 0);
             }
           }
         } else {
@@ -394,10 +397,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-            mma_ss(d_tmem, qa + off, kb + off, kIdS, kk > 0);
+            mma_ss_by(leader, d_tmem, qa + off, kb + off, kIdS, kk > 0);
           }
         }
-        mma_commit(smem_addr(&bars->s_full[i]));
+        mma_commit_by(leader, smem_addr(&bars->s_full[i]));
       };
       // O_i += P_i V_j over the K-steps [K0, K1) (16 keys each)
       auto issue_pv = [&](int i, int it, bool acc, auto k0_, auto k1_) {
@@ -413,7 +416,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t a_tmem = tmem + Cfg::kColS0 + i * 128;
 #pragma unroll
         for (int kk = K0; kk < K1; ++kk)
-          mma_ts(d_tmem, a_tmem + kk * 8, vb + kk * (2048 >> 4), kIdPV, (acc || kk > 0));
+          mma_ts_by(leader, d_tmem, a_tmem + kk * 8, vb + kk * (2048 >> 4), kIdPV, (acc || kk > 0));
       };
       using KAll0 = std::integral_constant<int, 0>;
       using KPart = std::integral_constant<int, kPvSteps0>;
@@ -425,9 +428,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int k = 0; ok && next_tile(p, k, t); ++k) {
         const int n_kv = max(t.n[0], t.n[1]);
         if (n_kv == 0) continue;  // no keys: the epilogue writes O = 0, LSE = -inf
-        ok = mbar_wait(smem_addr(&bars->q_full), qk & 1, lim);
+        ok = mbar_wait_warp(smem_addr(&bars->q_full), qk & 1, lim);
         ++qk;
-        if (ok) ok = mbar_wait(full_bar(0), full_phase(0), lim);
+        if (ok) ok = mbar_wait_warp(full_bar(0), full_phase(0), lim);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -435,7 +438,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (t.n[i] > 0) issue_s(i, 0);
         release(0);
         // Q is free again once the tile's last S MMA is done
-        if (n_kv == 1) mma_commit(smem_addr(&bars->q_empty));
+        if (n_kv == 1) mma_commit_by(leader, smem_addr(&bars->q_empty));
         for (int j = 0; j < n_kv; ++j) {
           const int itv = 2 * j + 1, itk = 2 * j + 2;
           const bool next_k = (j + 1) < n_kv;
@@ -444,22 +447,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           // released right after its last PV MMA, which gives the producer the
           // earliest start on the following loads.
           bool k_ready = !Cfg::kBlockRing || !next_k;
-          ok = mbar_wait(full_bar(itv), full_phase(itv), lim);
-          if (ok && next_k && !Cfg::kBlockRing) ok = mbar_wait(full_bar(itk), full_phase(itk), lim);
+          ok = mbar_wait_warp(full_bar(itv), full_phase(itv), lim);
+          if (ok && next_k && !Cfg::kBlockRing) ok = mbar_wait_warp(full_bar(itk), full_phase(itk), lim);
           if (!ok) break;
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             if (j >= t.n[i]) continue;
             if constexpr (kPvSteps0 < kTileN / 16) {
               // the first three quarters of P_i, then the rest
-              if (!mbar_wait(smem_addr(&bars->p_part[i]), pw[i] & 1, lim)) { ok = false; break; }
+              if (!mbar_wait_warp(smem_addr(&bars->p_part[i]), pw[i] & 1, lim)) { ok = false; break; }
               tc_fence_after();
               issue_pv(i, itv, j > 0, KAll0{}, KPart{});
-              if (!mbar_wait(smem_addr(&bars->p_full[i]), pw[i] & 1, lim)) { ok = false; break; }
+              if (!mbar_wait_warp(smem_addr(&bars->p_full[i]), pw[i] & 1, lim)) { ok = false; break; }
               tc_fence_after();
               issue_pv(i, itv, true, KPart{}, KAll1{});
             } else {
-              if (!mbar_wait(smem_addr(&bars->p_full[i]), pw[i] & 1, lim)) { ok = false; break; }
+              if (!mbar_wait_warp(smem_addr(&bars->p_full[i]), pw[i] & 1, lim)) { ok = false; break; }
               tc_fence_after();
               issue_pv(i, itv, j > 0, KAll0{}, KAll1{});
             }
@@ -470,10 +473,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // only the last PV of a tile is signalled (to the epilogue); earlier
             // ones are covered by the commit of the S MMA issued after them
             if (j + 1 == t.n[i]) {
-              mma_commit(smem_addr(&bars->pv_done[i]));
+              mma_commit_by(leader, smem_addr(&bars->pv_done[i]));
             } else {
               if (!k_ready) {
-                if (!(ok = mbar_wait(full_bar(itk), full_phase(itk), lim))) break;
+                if (!(ok = mbar_wait_warp(full_bar(itk), full_phase(itk), lim))) break;
                 k_ready = true;
               }
               issue_s(i, itk);
@@ -482,12 +485,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (!ok) break;
           if (!Cfg::kBlockRing) release(itv);
           if (next_k) release(itk);
-          if (j + 2 == n_kv) mma_commit(smem_addr(&bars->q_empty));
+          if (j + 2 == n_kv) mma_commit_by(leader, smem_addr(&bars->q_empty));
         }
         ld += 2 * n_kv;
         pos += n_kv * (kQB + kVB);
       }
-      if (!ok) record_error(p.err, kErrTimeout);
+      if (!ok && leader) record_error(p.err, kErrTimeout);
     }
   }
     __syncwarp();

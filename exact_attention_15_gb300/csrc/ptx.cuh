@@ -163,6 +163,43 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
+// The same three instructions issued by one lane of a warp that runs the issue
+// loop together: `leader` guards the instruction (no branch), so the operands
+// stay warp-uniform values.
+__device__ __forceinline__ void mma_ss_by(bool leader, uint32_t d_tmem, uint64_t a_desc,
+                                          uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, g;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 g, %5, 0;\n\t"
+      "@g tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(static_cast<uint32_t>(leader))
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_by(bool leader, uint32_t d_tmem, uint32_t a_tmem,
+                                          uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, g;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 g, %5, 0;\n\t"
+      "@g tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(static_cast<uint32_t>(leader))
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_by(bool leader, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred g;\n\t"
+      "setp.ne.b32 g, %1, 0;\n\t"
+      "@g tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+      "r"(static_cast<uint32_t>(leader))
+      : "memory");
+}
+// Bounded wait made by every lane of a warp; the result is the same in all
+// lanes (false if any lane ran out of time).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, long long limit) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit));
+}
+
 // Instruction descriptor for kind::f16 with bf16 operands and an fp32 accumulator.
 // a_mn / b_mn select MN-major ("transposed") operands; 0 means K-major.
 __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, int a_mn, int b_mn) {
