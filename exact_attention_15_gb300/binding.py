@@ -47,6 +47,7 @@ _SIGS = {
     "attn_set_fwd_variant": (_I, [_I]),
     "attn_debug_inject": (_I, [_I]),
     "attn_debug_stall": (_I, [_P]),
+    "attn_debug_rescale_stats": (_I, [_P, _I]),
     "attn_debug_fwd_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.c_longlong]),
     "attn_profile_enable": (_I, [_I]),
     "attn_profile_read": (_I, [_P, _I]),
@@ -162,6 +163,19 @@ def attn_debug_exp2(x, y, n, mode, stream) -> int:
 
 def attn_debug_inject(fault: int) -> int:
     return load().attn_debug_inject(int(fault))
+
+
+def attn_debug_rescale_stats(reset=True):
+    """The forward's rescale counters (a library built with ATTN_COUNT_RESCALE=1):
+    dict(warp_steps, warp_rescales, rows_moved, row_steps), or None when the
+    library has no counters."""
+    out = (ctypes.c_ulonglong * 4)()
+    n = load().attn_debug_rescale_stats(ctypes.cast(out, _P), int(bool(reset)))
+    if n < 0:
+        raise AttnError(-n, "attn_debug_rescale_stats")
+    if n == 0:
+        return None
+    return dict(warp_steps=out[0], warp_rescales=out[1], rows_moved=out[2], row_steps=out[3])
 
 
 def attn_debug_stall(stream=None) -> int:

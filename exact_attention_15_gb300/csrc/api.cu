@@ -29,6 +29,7 @@ cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int T, int H_q, int pa
                             int* seq_order, int* tile_start, int* err, cudaStream_t stream);
 cudaError_t launch_exp2_probe(const float* x, float* y, int n, int mode, cudaStream_t stream);
 cudaError_t launch_stall_probe(int* err, long long limit, cudaStream_t stream);
+int read_rescale_stats(unsigned long long* out, int reset);
 cudaError_t launch_attn_bwd(const BwdParams& p, const CUtensorMap* maps, cudaStream_t stream,
                             long long rows_q, int n_sem, int n_work);
 }  // namespace attn
@@ -871,6 +872,15 @@ int attn_debug_stall(attn_stream_t stream) {
                  cudaSuccess
              ? ATTN_OK
              : ATTN_ERR_CUDA;
+}
+
+int attn_debug_rescale_stats(unsigned long long* out, int reset) {
+  if (out == nullptr) return -ATTN_ERR_NULL_PTR;
+  int dev;
+  const int st = current_device(&dev);
+  if (st != ATTN_OK) return -st;
+  const int n = read_rescale_stats(out, reset);
+  return n < 0 ? -ATTN_ERR_CUDA : n;
 }
 
 int attn_debug_exp2(const float* x, float* y, int n, int mode, attn_stream_t stream) {

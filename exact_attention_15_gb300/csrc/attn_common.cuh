@@ -17,8 +17,18 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Conditional rescaling threshold, in powers of two: the running max used for
 // the exponentials is only moved when the true max has grown by more than
-// 2^8 = 256 (FlashAttention-4 summary, section 3.1.4).
-constexpr float kTau = 8.0f;
+// 2^8 = 256 (FlashAttention-4 summary, section 3.1.4). A measurement build may
+// set ATTN_TAU (0 rescales whenever the max grows, the baseline the pages
+// compare against); results differ only by rounding.
+#ifndef ATTN_TAU
+#define ATTN_TAU 8.0f
+#endif
+constexpr float kTau = ATTN_TAU;
+// ATTN_COUNT_RESCALE = 1 builds counters of the forward's rescale events
+// (attn_debug_rescale_stats); the shipped build has none.
+#ifndef ATTN_COUNT_RESCALE
+#define ATTN_COUNT_RESCALE 0
+#endif
 
 // Device error word values (the first failure is kept): a bounded wait ran
 // out; a packed-sequence offset array is not 0, non-decreasing, ..., T.

@@ -53,6 +53,13 @@ constexpr int kPWords0 = ATTN_FWD_P_WORDS0;
 static_assert(kPWords0 == 48 || kPWords0 == 64, "P split: three quarters or none");
 constexpr int kPvSteps0 = kPWords0 / 8;  // PV K-steps (16 keys each) on the first part
 
+#if ATTN_COUNT_RESCALE
+// [0] (warp, key tile) softmax steps after a row's first key tile, [1] those
+// steps in which the warp rescaled (some row's bias moved), [2] rows whose
+// bias moved, [3] row steps counted
+__device__ unsigned long long g_rescale_stats[4];
+#endif
+
 // Shared-memory plan. Q/K rows have DQK columns, V/O rows DV columns; every
 // tile is stored as 128-row x 64-column (16 KB) 128-byte-swizzled blocks.
 // Equal head dimensions: K and V share a ring of single-tile stages (load order
@@ -539,6 +546,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                         rescale_warp, factor)
                 : softmax_row_max<false>(s, c, m_used, l, kv0, qrow, Lk, need_mask, p.causal,
                                          rescale_warp, factor);
+#if ATTN_COUNT_RESCALE
+        if (j > 0) {
+          const unsigned moved = __ballot_sync(0xffffffffu, rescale_warp && factor != 1.0f);
+          if ((r & 31) == 0) {
+            atomicAdd(&g_rescale_stats[0], 1ull);
+            if (moved) atomicAdd(&g_rescale_stats[1], 1ull);
+            atomicAdd(&g_rescale_stats[2], static_cast<unsigned long long>(__popc(moved)));
+            atomicAdd(&g_rescale_stats[3], 32ull);
+          }
+        }
+#endif
         uint64_t sum2[2] = {0ull, 0ull};
         if (pos) softmax_row_exp<EMU, true, 0, kPWords0>(s, c, mb, need_mask, pk, sum2);
         else softmax_row_exp<0, false, 0, kPWords0>(s, c, mb, need_mask, pk, sum2);
@@ -756,6 +774,23 @@ cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int T, int H_q, int pa
   e = cudaGetLastError();
   prof_end(slot, stream);
   return e;
+}
+
+// Reads (and with reset clears) the rescale counters; returns the number of
+// values written (0 when the library was built without them).
+int read_rescale_stats(unsigned long long* out, int reset) {
+#if ATTN_COUNT_RESCALE
+  if (cudaMemcpyFromSymbol(out, g_rescale_stats, sizeof(g_rescale_stats)) != cudaSuccess) return -1;
+  if (reset) {
+    const unsigned long long z[4] = {0ull, 0ull, 0ull, 0ull};
+    if (cudaMemcpyToSymbol(g_rescale_stats, z, sizeof(z)) != cudaSuccess) return -1;
+  }
+  return 4;
+#else
+  (void)out;
+  (void)reset;
+  return 0;
+#endif
 }
 
 // ------------------------------------------------------------------ exp2 test hook

@@ -260,6 +260,20 @@ const char* attn_status_string(int status);
 int attn_debug_exp2(const float* x, float* y, int n, int mode, attn_stream_t stream);
 
 /*
+ * Measurement hook for the forward's conditional rescaling (FlashAttention-4
+ * summary, section 3.1.4; the Korean FA-4 review reports about 10x fewer
+ * rescales than rescaling whenever the max grows). In a library built with
+ * ATTN_COUNT_RESCALE=1 the forward kernels count, over all calls since the last
+ * reset, out[0] the (warp, key tile) softmax steps after each row's first key
+ * tile, out[1] those steps in which the warp rescaled O and l, out[2] the rows
+ * whose exponent bias moved, out[3] the row steps counted. Writes the four
+ * counts into out (4 entries) and returns 4, clearing them when reset != 0;
+ * returns 0 without touching out in the shipped build, which has no counters;
+ * a negative attn_status on failure. Synchronous (waits for the device).
+ */
+int attn_debug_rescale_stats(unsigned long long* out, int reset);
+
+/*
  * Failure-path test hooks. They exercise the bounded device-side waits without
  * faulting, trapping or hanging the GPU.
  *

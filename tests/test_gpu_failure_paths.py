@@ -52,3 +52,10 @@ def test_skipped_semaphore_release_times_out_then_recovers():
     for a, b in zip(ref, again):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     _ = (np, GRAD_TOL, rel_fro, to_host_f64)
+
+
+def test_rescale_counters_absent_in_shipped_build():
+    """The forward's rescale counters exist only in a measurement build
+    (ATTN_COUNT_RESCALE=1); the shipped library reports none."""
+    from exact_attention_15_gb300 import binding
+    assert binding.attn_debug_rescale_stats() is None
