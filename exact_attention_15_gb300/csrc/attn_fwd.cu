@@ -85,6 +85,12 @@ struct FwdCfg {
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // barriers + alignment slack
   static constexpr uint32_t kColO0 = 0, kColO1 = DV;
   static constexpr uint32_t kColS0 = 2 * DV, kColS1 = 2 * DV + 128;
+  // d = 64: O (64 columns each) leaves room for P in its own columns (bf16
+  // pairs, 64 each) beside S, so S of the next key tile can be computed while
+  // the softmax still turns the current one into P; otherwise P overwrites S.
+  static constexpr bool kSepP = DQK == 64 && DV == 64;
+  static constexpr uint32_t kColP0 = kSepP ? 2 * DV + 256 : kColS0;
+  static constexpr uint32_t kColPStep = kSepP ? 64 : 128;  // P_1 = P_0 + kColPStep
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
@@ -114,7 +120,8 @@ struct FwdBars {
   uint64_t s_full[2];
   uint64_t p_part[2];   // the first kPWords0 packed P words of the row are in TMEM
   uint64_t p_full[2];   // all of P is in TMEM
-  uint64_t pv_done[2];
+  uint64_t pv_done[2];   // O_t complete (last PV of a tile; every PV with a separate P)
+  uint64_t s_free[2];    // separate P: the softmax has S_t in registers
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
   uint32_t tmem_base;
@@ -230,6 +237,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(smem_addr(&bars->p_part[i]), 128);
       mbar_init(smem_addr(&bars->p_full[i]), 128);
       mbar_init(smem_addr(&bars->pv_done[i]), 1);
+      mbar_init(smem_addr(&bars->s_free[i]), 128);
     }
     // tile ring: kv_full / kv_empty per stage; block ring: kv_full per load in
     // flight, kv_empty per slot
@@ -420,7 +428,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           vb = v_desc + ((stage_of(it) * Cfg::kTileBytes) >> 4);
         }
         const uint32_t d_tmem = tmem + Cfg::kColO0 + i * DV;
-        const uint32_t a_tmem = tmem + Cfg::kColS0 + i * 128;
+        const uint32_t a_tmem = tmem + Cfg::kColP0 + i * Cfg::kColPStep;
 #pragma unroll
         for (int kk = K0; kk < K1; ++kk)
           mma_ts_by(leader, d_tmem, a_tmem + kk * 8, vb + kk * (2048 >> 4), kIdPV, (acc || kk > 0));
@@ -432,6 +440,76 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       int qk = 0;          // tiles with a Q load
       bool ok = true;
       FwdTile t;
+      if constexpr (Cfg::kSepP) {
+        // P in its own TMEM columns: S_i of key tile j + 1 is issued once the
+        // softmax warpgroup has S_i(j) in registers (s_free), before P_i(j) is
+        // ready, so the tensor core computes the next scores while the
+        // softmax runs (the order of the four MMAs of a key tile depends on
+        // the mask, below), and every PV is committed to pv_done (the softmax
+        // waits for PV_i(j) before it writes P_i(j+1) into the same columns).
+        int sf[2] = {0, 0};  // s_free waits so far, per query tile
+        int ns[2] = {0, 0};  // S MMAs issued so far, per query tile
+        auto wait_free_issue_s = [&](int i, int it) {
+          if (ns[i] > 0) {  // the softmax has read the previous S_i
+            if (!mbar_wait_warp(smem_addr(&bars->s_free[i]), sf[i] & 1, lim)) return false;
+            ++sf[i];
+            tc_fence_after();
+          }
+          issue_s(i, it);
+          ++ns[i];
+          return true;
+        };
+        for (int k = 0; ok && next_tile(p, k, t); ++k) {
+          const int n_kv = max(t.n[0], t.n[1]);
+          if (n_kv == 0) continue;  // no keys: the epilogue writes O = 0, LSE = -inf
+          ok = mbar_wait_warp(smem_addr(&bars->q_full), qk & 1, lim);
+          ++qk;
+          if (ok) ok = mbar_wait_warp(full_bar(0), full_phase(0), lim);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            if (ok && t.n[i] > 0) ok = wait_free_issue_s(i, 0);
+          if (!ok) break;
+          release(0);
+          if (n_kv == 1) mma_commit_by(leader, smem_addr(&bars->q_empty));
+          for (int j = 0; j < n_kv; ++j) {
+            const int itv = 2 * j + 1, itk = 2 * j + 2;
+            const bool next_k = j + 1 < n_kv;
+            if (next_k && !(ok = mbar_wait_warp(full_bar(itk), full_phase(itk), lim))) break;
+            if (!(ok = mbar_wait_warp(full_bar(itv), full_phase(itv), lim))) break;
+            auto s_next = [&](int i) {  // S_i(j+1), once the softmax has S_i(j)
+              if (ok && j + 1 < t.n[i]) ok = wait_free_issue_s(i, itk);
+            };
+            auto pv_now = [&](int i) {  // O_i += P_i(j) V_j
+              if (!ok || j >= t.n[i]) return;
+              if (!(ok = mbar_wait_warp(smem_addr(&bars->p_full[i]), pw[i] & 1, lim))) return;
+              ++pw[i];
+              tc_fence_after();
+              issue_pv(i, itv, j > 0, KAll0{}, KAll1{});
+              mma_commit_by(leader, smem_addr(&bars->pv_done[i]));
+            };
+            if (p.causal) {
+              // S_0(j+1), S_1(j+1), PV_0(j), PV_1(j): the two query tiles of a
+              // causal work tile see different key counts and masks, which
+              // already keeps their softmax warpgroups apart
+              s_next(0); s_next(1); pv_now(0); pv_now(1);
+            } else {
+              // S_0(j+1), PV_0(j), S_1(j+1), PV_1(j): query tile 1's S waits
+              // behind query tile 0's PV, which staggers two equal query
+              // tiles by about one PV + S instead of letting their softmax
+              // warpgroups run in lockstep and compete for issue slots
+              s_next(0); pv_now(0); s_next(1); pv_now(1);
+            }
+            if (!ok) break;
+            if (next_k) release(itk);  // after the last S reading K_{j+1}
+            release(itv);              // after the last PV reading V_j
+            // Q is free again once the tile's last S MMA is done
+            if (j + 2 == n_kv) mma_commit_by(leader, smem_addr(&bars->q_empty));
+          }
+          ld += 2 * n_kv;
+        }
+      } else
       for (int k = 0; ok && next_tile(p, k, t); ++k) {
         const int n_kv = max(t.n[0], t.n[1]);
         if (n_kv == 0) continue;  // no keys: the epilogue writes O = 0, LSE = -inf
@@ -509,9 +587,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t lane_base = static_cast<uint32_t>((r & ~31)) << 16;
     const uint32_t col_s = i ? Cfg::kColS1 : Cfg::kColS0;
     const uint32_t col_o = i ? Cfg::kColO1 : Cfg::kColO0;
+    const uint32_t col_p = Cfg::kColP0 + i * Cfg::kColPStep;  // P (over S unless kSepP)
     const float c = p.scale_log2;
     int sw = 0;   // s_full waits so far
     int pvw = 0;  // pv_done waits so far
+    int pvc = 0;  // separate P: PV MMAs of this query tile in earlier work tiles
     bool ok = true;
     for (int k = 0; ok; ++k) {
       FwdTile t;
@@ -534,6 +614,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_ld32(tmem + lane_base + col_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + cc * 32));
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(sr + cc * 32));
+        }
+        if constexpr (Cfg::kSepP) {
+          // S_i(j) is in registers: the MMA warp may write S_i(j + 1) now
+          tc_fence_before();
+          mbar_arrive(smem_addr(&bars->s_free[i]));
         }
         const int kv0 = j * kTileN;
         const bool need_mask = (kv0 + kTileN > Lk) || (p.causal && kv0 + kTileN - 1 > q0i);
@@ -560,11 +645,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         uint64_t sum2[2] = {0ull, 0ull};
         if (pos) softmax_row_exp<EMU, true, 0, kPWords0>(s, c, mb, need_mask, pk, sum2);
         else softmax_row_exp<0, false, 0, kPWords0>(s, c, mb, need_mask, pk, sum2);
+        if (Cfg::kSepP && j > 0) {
+          // PV_i(j - 1) has read P_i(j - 1) and finished O_{j-1}. Waiting on its
+          // own phase is unambiguous: S_i(j) completed, and it was issued after
+          // PV_i(j - 2), so at most this one PV is outstanding.
+          if (!mbar_wait(smem_addr(&bars->pv_done[i]), (pvc + j - 1) & 1, lim)) { ok = false; break; }
+          tc_fence_after();
+        }
         if (rescale_warp && j > 0 && __any_sync(0xffffffffu, factor != 1.0f)) {
-          // correction: O_{j-1} is complete here, because the commit that
+          // correction: O_{j-1} is complete here (P over S: the commit that
           // signalled S_j came from the thread that issued PV_{j-1} before S_j;
-          // it is back in TMEM before the first part of P is signalled, so
-          // before PV_j adds to O
+          // separate P: the wait above); it is back in TMEM before the first
+          // part of P is signalled, so before PV_j adds to O
 #pragma unroll
           for (int cc = 0; cc < DV / 32; ++cc) {
             uint32_t ov[32];
@@ -575,8 +667,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_st32(tmem + lane_base + col_o + cc * 32, ov);
           }
         }
-        tmem_st32(tmem + lane_base + col_s, *reinterpret_cast<uint32_t(*)[32]>(pk));
-        if constexpr (kPWords0 < 64) {
+        tmem_st32(tmem + lane_base + col_p, *reinterpret_cast<uint32_t(*)[32]>(pk));
+        if constexpr (kPWords0 < 64 && !Cfg::kSepP) {
           tmem_st16(tmem + lane_base + col_s + 32, *reinterpret_cast<uint32_t(*)[16]>(pk + 32));
           tmem_st_wait();
           tc_fence_before();
@@ -585,7 +677,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           else softmax_row_exp<0, false, kPWords0, 64>(s, c, mb, need_mask, pk, sum2);
           tmem_st16(tmem + lane_base + col_s + 48, *reinterpret_cast<uint32_t(*)[16]>(pk + 48));
         } else {
-          tmem_st32(tmem + lane_base + col_s + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+          tmem_st32(tmem + lane_base + col_p + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
         }
         tmem_st_wait();
         tc_fence_before();
@@ -599,7 +691,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (i ? t.valid[1] : t.valid[0]) {
         bool have_o = my_n > 0;
         if (have_o) {
-          have_o = mbar_wait(smem_addr(&bars->pv_done[i]), pvw & 1, lim);
+          // the tile's last PV (separate P: every PV is committed, so the
+          // phase is that PV's own)
+          have_o = mbar_wait(smem_addr(&bars->pv_done[i]),
+                             Cfg::kSepP ? (pvc + my_n - 1) & 1 : pvw & 1, lim);
           ++pvw;
           if (!have_o) { ok = false; break; }
           tc_fence_after();
@@ -640,6 +735,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           p.lse[l_off] = lse;
         }
       }
+      pvc += my_n;
     }
     if (!ok) record_error(p.err, kErrTimeout);
   }
