@@ -838,16 +838,20 @@ static cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk,
   return e;
 }
 
-// Number of exponentials per 8 pairs routed to the FMA polynomial.
+// Number of exponentials per 8 pairs routed to the FMA polynomial (d = 64 has
+// its own setting).
 #ifndef ATTN_FWD_EMU
 #define ATTN_FWD_EMU 0
+#endif
+#ifndef ATTN_FWD_EMU_64
+#define ATTN_FWD_EMU_64 ATTN_FWD_EMU
 #endif
 
 // Supported (d_qk, d_v): (64, 64), (128, 128), (192, 128); the caller checks.
 cudaError_t launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const FwdParams& p, dim3 grid,
                             cudaStream_t stream) {
-  if (d_qk == 64 && d_v == 64) return launch_fwd_impl<64, 64, ATTN_FWD_EMU>(tq, tk, tv, p, grid, stream);
+  if (d_qk == 64 && d_v == 64) return launch_fwd_impl<64, 64, ATTN_FWD_EMU_64>(tq, tk, tv, p, grid, stream);
   if (d_qk == 192 && d_v == 128)
     return launch_fwd_impl<192, 128, ATTN_FWD_EMU>(tq, tk, tv, p, grid, stream);
   return launch_fwd_impl<128, 128, ATTN_FWD_EMU>(tq, tk, tv, p, grid, stream);
@@ -893,7 +897,14 @@ int read_rescale_stats(unsigned long long* out, int reset) {
 __global__ void exp2_probe_kernel(const float* __restrict__ x, float* __restrict__ y, int n,
                                   int mode) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) y[i] = mode ? exp2_poly3(x[i]) : ex2_approx(x[i]);
+  if (i < n) {
+    if (mode) {
+      float y1;
+      exp2_poly3_x2(x[i], x[i], y[i], y1);
+    } else {
+      y[i] = ex2_approx(x[i]);
+    }
+  }
 }
 
 // Failure test: one CTA waits on an mbarrier that nothing ever arrives at. The

@@ -5,7 +5,7 @@ term is pinned to 1 so that p(0) = 1 exactly, as the FlashAttention-4 summary,
 section 3.1.3, describes). The coefficients minimise the maximum relative
 error (minimax) and are found with a Remez exchange on the relative error, in
 float64, then rounded to float32. Run as a script to print them; the values are
-the constants of ``exp2_poly3`` in ``attn_common.cuh``.
+the constants of ``exp2_poly3_x2`` in ``attn_common.cuh``.
 """
 
 import numpy as np

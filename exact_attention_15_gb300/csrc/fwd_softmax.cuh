@@ -78,8 +78,7 @@ __device__ __forceinline__ void softmax_row_exp(const float (&s)[128], float c, 
     f32x2_split(POS_SCALE ? fma_f32x2(s2, c2, nb2) : add_f32x2(s2, nb2), x0, x1);
     float p0, p1;
     if (EMU > 0 && !need_mask && (i & 7) >= 8 - EMU) {
-      p0 = exp2_poly3(x0);
-      p1 = exp2_poly3(x1);
+      exp2_poly3_x2(x0, x1, p0, p1);
     } else {
       p0 = ex2_approx(x0);
       p1 = ex2_approx(x1);
