@@ -313,7 +313,10 @@ attn_bwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     } else if (warp == 1) {
       // ------------------------------------------------------- MMA issuer (CTA 0)
       // Per query tile: dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1} (after S_0, dP_0).
-      if (rank == 0 && lane == 0 && n_it > 0) {
+      if (rank == 0 && n_it > 0) {
+        // the whole warp runs the issue loop; one elected lane issues each
+        // MMA and commit
+        const bool issuer = elect_one_sync();
         constexpr uint32_t kIdSS = make_idesc_bf16(256, 128, 0, 0);  // S^T, dP^T
         constexpr uint32_t kIdTS = make_idesc_bf16(256, D, 0, 1);    // dV, dK: B MN-major
         constexpr uint32_t kIdDQ = make_idesc_bf16(128, D, 1, 1);    // dQ: A, B MN-major
@@ -333,23 +336,23 @@ attn_bwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           const uint64_t qb = qr_km + (it & 1) * (Cfg::kBlk >> 4);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss_pair(tmem + Cfg::kColS, k_km + koff(kk), qb + koff_h(kk), kIdSS, kk > 0);
-          mma_commit_pair(smem_addr(&bars->s_full));
+            mma_ss_pair_by(issuer, tmem + Cfg::kColS, k_km + koff(kk), qb + koff_h(kk), kIdSS, kk > 0);
+          mma_commit_pair_by(issuer, smem_addr(&bars->s_full));
         };
         auto issue_dp = [&]() {  // dP^T = V dO^T
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss_pair(tmem + Cfg::kColDP, v_km + koff(kk), dor_km + koff_h(kk), kIdSS, kk > 0);
-          mma_commit_pair(smem_addr(&bars->dp_full));
-          mma_commit_pair(smem_addr(&bars->do_r_empty));
+            mma_ss_pair_by(issuer, tmem + Cfg::kColDP, v_km + koff(kk), dor_km + koff_h(kk), kIdSS, kk > 0);
+          mma_commit_pair_by(issuer, smem_addr(&bars->dp_full));
+          mma_commit_pair_by(issuer, smem_addr(&bars->do_r_empty));
         };
-        bool ok = mbar_wait_cluster(smem_addr(&bars->kv_full), 0, lim);
-        if (ok) ok = mbar_wait_cluster(smem_addr(&bars->q_full[0]), 0, lim);
+        bool ok = mbar_wait_cluster_warp(smem_addr(&bars->kv_full), 0, lim);
+        if (ok) ok = mbar_wait_cluster_warp(smem_addr(&bars->q_full[0]), 0, lim);
         if (ok) {
           tc_fence_after();
           issue_s(0);
         }
-        if (ok) ok = mbar_wait_cluster(smem_addr(&bars->do_r_full), 0, lim);
+        if (ok) ok = mbar_wait_cluster_warp(smem_addr(&bars->do_r_full), 0, lim);
         if (ok) {
           tc_fence_after();
           issue_dp();
@@ -357,51 +360,51 @@ attn_bwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         for (int it = 0; ok && it < n_it; ++it) {
           const int stage = it & 1;
           // dV += P^T dO: P^T of query half s sits in S^T columns [64 s, 64 s + 32)
-          if (!(ok = mbar_wait_cluster(smem_addr(&bars->p_ready), it & 1, lim))) break;
-          if (!(ok = mbar_wait_cluster(smem_addr(&bars->do_c_full), it & 1, lim))) break;
+          if (!(ok = mbar_wait_cluster_warp(smem_addr(&bars->p_ready), it & 1, lim))) break;
+          if (!(ok = mbar_wait_cluster_warp(smem_addr(&bars->do_c_full), it & 1, lim))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk)
-            mma_ts_pair(tmem + Cfg::kColDV, tmem + Cfg::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
+            mma_ts_pair_by(issuer, tmem + Cfg::kColDV, tmem + Cfg::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
                         doc_mn + kk * (2048 >> 4), kIdTS, (it > 0 || kk > 0));
-          mma_commit_pair(smem_addr(&bars->do_c_empty));
+          mma_commit_pair_by(issuer, smem_addr(&bars->do_c_empty));
           // S^T of the next query tile into the same columns (MMAs run in issue
           // order: dV has read P^T first)
           if (it + 1 < n_it) {
-            if (!(ok = mbar_wait_cluster(smem_addr(&bars->q_full[(it + 1) & 1]), ((it + 1) >> 1) & 1, lim)))
+            if (!(ok = mbar_wait_cluster_warp(smem_addr(&bars->q_full[(it + 1) & 1]), ((it + 1) >> 1) & 1, lim)))
               break;
             tc_fence_after();
             issue_s(it + 1);
           }
           // dK += dS^T Q (dS^T in TMEM over dP^T); dQ = dS K over both CTAs' keys
-          if (!(ok = mbar_wait_cluster(smem_addr(&bars->ds_ready), it & 1, lim))) break;
-          if (!(ok = mbar_wait_cluster(smem_addr(&bars->qc_full), it & 1, lim))) break;
+          if (!(ok = mbar_wait_cluster_warp(smem_addr(&bars->ds_ready), it & 1, lim))) break;
+          if (!(ok = mbar_wait_cluster_warp(smem_addr(&bars->qc_full), it & 1, lim))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kTileM / 16; ++kk)
-            mma_ts_pair(tmem + Cfg::kColDK, tmem + Cfg::kColDP + (kk >> 2) * 64 + (kk & 3) * 8,
+            mma_ts_pair_by(issuer, tmem + Cfg::kColDK, tmem + Cfg::kColDP + (kk >> 2) * 64 + (kk & 3) * 8,
                         qc_mn + kk * (2048 >> 4), kIdTS, (it > 0 || kk > 0));
-          mma_commit_pair(smem_addr(&bars->qc_empty));
+          mma_commit_pair_by(issuer, smem_addr(&bars->qc_empty));
 #pragma unroll
           for (int kk = 0; kk < 2 * kTileN / 16; ++kk) {
             // key step kk: keys of CTA kk / 8, rows 16 (kk % 8) ..
             const uint32_t off = ((kk >> 3) * Cfg::kBlk + (kk & 7) * 2048) >> 4;
-            mma_ss_pair(tmem + Cfg::kColDP, rk_mn + off, bk_mn + off, kIdDQ, kk > 0);
+            mma_ss_pair_by(issuer, tmem + Cfg::kColDP, rk_mn + off, bk_mn + off, kIdDQ, kk > 0);
           }
-          mma_commit_pair(smem_addr(&bars->dq_full));  // covers every earlier MMA, dV included
-          mma_commit_pair(smem_addr(&bars->q_empty[stage]));
+          mma_commit_pair_by(issuer, smem_addr(&bars->dq_full));  // covers every earlier MMA, dV included
+          mma_commit_pair_by(issuer, smem_addr(&bars->q_empty[stage]));
           // dP^T of the next tile reuses the dQ columns once dQ_i has been read out
           if (it + 1 < n_it) {
-            if (!(ok = mbar_wait_cluster(smem_addr(&bars->dq_free), it & 1, lim))) break;
-            if (!(ok = mbar_wait_cluster(smem_addr(&bars->do_r_full), (it + 1) & 1, lim))) break;
+            if (!(ok = mbar_wait_cluster_warp(smem_addr(&bars->dq_free), it & 1, lim))) break;
+            if (!(ok = mbar_wait_cluster_warp(smem_addr(&bars->do_r_full), (it + 1) & 1, lim))) break;
             tc_fence_after();
             issue_dp();
           }
         }
         // a last commit, after which no arrival of this pair's MMAs is pending
         // in either CTA
-        if (ok) mma_commit_pair(smem_addr(&bars->fin));
-        if (!ok) record_error(p.err, kErrTimeout);
+        if (ok) mma_commit_pair_by(issuer, smem_addr(&bars->fin));
+        if (!ok && issuer) record_error(p.err, kErrTimeout);
       }
       if (lane == 0 && n_it > 0 && !mbar_wait(smem_addr(&bars->fin), 0, lim))
         record_error(p.err, kErrTimeout);

@@ -256,12 +256,15 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer (even CTA)
-      if (rank == 0 && lane == 0 && n_kv > 0) {
+      if (rank == 0 && n_kv > 0) {
+        // the whole warp runs the issue loop; one elected lane issues each
+        // MMA and commit
+        const bool issuer = elect_one_sync();
         constexpr uint32_t kIdS = make_idesc_bf16(256, 128, 0, 0);
         constexpr uint32_t kIdPV = make_idesc_bf16(256, D, 0, 1);
         const uint32_t q_base = smem_addr(smem + Cfg::kQOff);
         const uint32_t kv_base = smem_addr(smem + Cfg::kKVOff);
-        bool ok = mbar_wait_cluster(smem_addr(&bars->q_full), 0, lim);
+        bool ok = mbar_wait_cluster_warp(smem_addr(&bars->q_full), 0, lim);
         const uint64_t q_desc = make_sdesc_sw128(q_base, 16, 1024);      // K-major, 128 rows
         const uint64_t k_desc = make_sdesc_sw128(kv_base, 16, 1024);     // K-major, 64 rows
         const uint64_t v_desc = make_sdesc_sw128(kv_base, 16384, 1024);  // MN-major, 64 columns
@@ -274,10 +277,10 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             // Q: 16 KB per 64-column block of 128 rows; K half: 8 KB per block of 64 rows
-            mma_ss_pair(d_tmem, qa + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
+            mma_ss_pair_by(issuer, d_tmem, qa + (((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
                         kb + (((kk >> 2) * 8192 + (kk & 3) * 32) >> 4), kIdS, kk > 0);
           }
-          mma_commit_pair(smem_addr(&bars->s_full[s]));
+          mma_commit_pair_by(issuer, smem_addr(&bars->s_full[s]));
         };
         auto issue_pv = [&](int s, int stage, int j) {
           const uint64_t vb = v_desc + ((stage * Cfg::kHalfBytes) >> 4);
@@ -285,37 +288,37 @@ attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
           const uint32_t a_tmem = tmem + Cfg::kColS0 + s * 128;
 #pragma unroll
           for (int kk = 0; kk < kTileN / 16; ++kk)
-            mma_ts_pair(d_tmem, a_tmem + kk * 8, vb + kk * (2048 >> 4), kIdPV, (j > 0 || kk > 0));
-          if (j + 1 == t.n[s]) mma_commit_pair(smem_addr(&bars->pv_done[s]));
+            mma_ts_pair_by(issuer, d_tmem, a_tmem + kk * 8, vb + kk * (2048 >> 4), kIdPV, (j > 0 || kk > 0));
+          if (j + 1 == t.n[s]) mma_commit_pair_by(issuer, smem_addr(&bars->pv_done[s]));
         };
-        if (ok) ok = mbar_wait_cluster(smem_addr(&bars->kv_full[stage_of(0)]), phase_of(0), lim);
+        if (ok) ok = mbar_wait_cluster_warp(smem_addr(&bars->kv_full[stage_of(0)]), phase_of(0), lim);
         if (ok) {
           tc_fence_after();
 #pragma unroll
           for (int s = 0; s < 2; ++s)
             if (t.n[s] > 0) issue_s(s, stage_of(0));
-          mma_commit_pair(smem_addr(&bars->kv_empty[stage_of(0)]));
+          mma_commit_pair_by(issuer, smem_addr(&bars->kv_empty[stage_of(0)]));
         }
         for (int j = 0; ok && j < n_kv; ++j) {
           const int itv = 2 * j + 1, itk = 2 * j + 2;
           const bool next_k = (j + 1) < n_kv;
-          ok = mbar_wait_cluster(smem_addr(&bars->kv_full[stage_of(itv)]), phase_of(itv), lim);
+          ok = mbar_wait_cluster_warp(smem_addr(&bars->kv_full[stage_of(itv)]), phase_of(itv), lim);
           if (ok && next_k)
-            ok = mbar_wait_cluster(smem_addr(&bars->kv_full[stage_of(itk)]), phase_of(itk), lim);
+            ok = mbar_wait_cluster_warp(smem_addr(&bars->kv_full[stage_of(itk)]), phase_of(itk), lim);
           if (!ok) break;
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
             if (j >= t.n[s]) continue;
-            if (!mbar_wait_cluster(smem_addr(&bars->p_full[s]), j & 1, lim)) { ok = false; break; }
+            if (!mbar_wait_cluster_warp(smem_addr(&bars->p_full[s]), j & 1, lim)) { ok = false; break; }
             tc_fence_after();
             issue_pv(s, stage_of(itv), j);
             if (j + 1 < t.n[s]) issue_s(s, stage_of(itk));
           }
           if (!ok) break;
-          mma_commit_pair(smem_addr(&bars->kv_empty[stage_of(itv)]));
-          if (next_k) mma_commit_pair(smem_addr(&bars->kv_empty[stage_of(itk)]));
+          mma_commit_pair_by(issuer, smem_addr(&bars->kv_empty[stage_of(itv)]));
+          if (next_k) mma_commit_pair_by(issuer, smem_addr(&bars->kv_empty[stage_of(itk)]));
         }
-        if (!ok) record_error(p.err, kErrTimeout);
+        if (!ok && issuer) record_error(p.err, kErrTimeout);
       }
     }
     __syncwarp();

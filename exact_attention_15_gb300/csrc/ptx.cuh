@@ -462,6 +462,44 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
       "h"(static_cast<unsigned short>(3))
       : "memory");
 }
+// The pair instructions issued by one lane of a warp that runs the issue loop
+// together (`leader` guards the instruction, see mma_ss_by).
+__device__ __forceinline__ void mma_ss_pair_by(bool leader, uint32_t d_tmem, uint64_t a_desc,
+                                               uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, g;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 g, %5, 0;\n\t"
+      "@g tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(static_cast<uint32_t>(leader))
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_pair_by(bool leader, uint32_t d_tmem, uint32_t a_tmem,
+                                               uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, g;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.ne.b32 g, %5, 0;\n\t"
+      "@g tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(static_cast<uint32_t>(leader))
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_pair_by(bool leader, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred g;\n\t"
+      "setp.ne.b32 g, %2, 0;\n\t"
+      "@g tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}" ::"r"(bar),
+      "h"(static_cast<unsigned short>(3)), "r"(static_cast<uint32_t>(leader))
+      : "memory");
+}
+// Bounded cluster-scope wait made by every lane of a warp (same result in all
+// lanes).
+__device__ __forceinline__ bool mbar_wait_cluster_warp(uint32_t bar, uint32_t parity, long long limit) {
+  return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity, limit));
+}
 // 16-byte store into shared memory of a CTA of the cluster (cluster address).
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
