@@ -185,6 +185,7 @@ def attn_debug_stall(stream=None) -> int:
 FWD_ONE_CTA_PER_TILE = 0
 FWD_STRIDING = 1
 FWD_BALANCED_LIST = 2
+FWD_CLAIMED = 3
 
 
 def attn_debug_fwd_plan(B, H_q, H_kv, N_q, N_k, d_qk, d_v, causal, varlen, n_sm, want_lists=True):

@@ -26,7 +26,8 @@ cudaError_t launch_attn_fwd_pair(const CUtensorMap& tq, const CUtensorMap& tk_ha
                                  const CUtensorMap& tv, const FwdParams& p, dim3 grid,
                                  cudaStream_t stream);
 cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int T, int H_q, int pair_heads,
-                            int* seq_order, int* tile_start, int* err, cudaStream_t stream);
+                            int* seq_order, int* tile_start, int* tile_ctr, int* err,
+                            cudaStream_t stream);
 cudaError_t launch_exp2_probe(const float* x, float* y, int n, int mode, cudaStream_t stream);
 cudaError_t launch_stall_probe(int* err, long long limit, cudaStream_t stream);
 int read_rescale_stats(unsigned long long* out, int reset);
@@ -105,9 +106,9 @@ int sm_count(int dev) {
 }
 
 // Work-list metadata of the forward for packed sequences, one buffer per
-// (device, stream): the sequence order and the first work tile of each
-// sequence, written by the plan kernel right before the forward that reads
-// them. Launches on one stream run in order, so they can share it; launches on
+// (device, stream): the sequence order, the first work tile of each sequence
+// and the claim counter of the forward's schedule, written by the plan kernel
+// right before the forward that reads them. Launches on one stream run in order, so they can share it; launches on
 // different streams get different buffers. Buffers live until the process exits.
 struct PlanBuf {
   int dev;
@@ -128,7 +129,7 @@ int plan_buffer(int dev, cudaStream_t stream, int seqs, PlanBuf* out) {
     return ATTN_OK;
   }
   const int cap = seqs > 1024 ? seqs : 1024;
-  const size_t bytes = (2 * static_cast<size_t>(cap) + 1) * sizeof(int);
+  const size_t bytes = (2 * static_cast<size_t>(cap) + 2) * sizeof(int);
   if (found) {
     // growing: earlier launches on this stream may still read the old buffer
     if (cudaStreamSynchronize(stream) != cudaSuccess || cudaFree(found->ptr) != cudaSuccess)
@@ -295,7 +296,7 @@ int l2_section_heads(int H_q, int H_kv, long long rows, int width) {
 // tile (kFwdOneCtaPerTile, kFwdStriding, kFwdBalancedList). The balanced list
 // is the intent; a call falls back to one CTA per tile when the list cannot be
 // made at that moment (stream capture of a new shape, or the shape cache full).
-enum { kFwdOneCtaPerTile = 0, kFwdStriding = 1, kFwdBalancedList = 2 };
+enum { kFwdOneCtaPerTile = 0, kFwdStriding = 1, kFwdBalancedList = 2, kFwdClaimed = 3 };
 struct FwdPlan {
   long long tiles;  // exact for fixed length, an upper bound when packed
   int pair;         // work tiles of two query heads (causal, even GQA group)
@@ -321,7 +322,12 @@ FwdPlan fwd_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d_qk, int d_v, 
   f.sec_heads = l2_section_heads(H_q, H_kv, varlen ? (N_k + B - 1) / B : N_k, d_qk + d_v);
   f.mode = kFwdOneCtaPerTile;
   f.grid = f.tiles;
-  if (f.tiles > n_sm) {
+  if (f.tiles > n_sm && varlen) {
+    // packed: the tiles' sizes are known only on the device, so one CTA per SM
+    // claims tiles from a counter as it finishes them (greedy list scheduling)
+    f.mode = kFwdClaimed;
+    f.grid = n_sm;
+  } else if (f.tiles > n_sm) {
     if (fwd_persistent(f.tiles, n_sm, causal, varlen, varlen ? (N_k + B - 1) / B : N_k,
                        d_qk + d_v)) {
       f.mode = kFwdStriding;
@@ -642,6 +648,7 @@ int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* l
   p.tile_start = nullptr;
   p.tile_list = nullptr;
   p.cta_start = nullptr;
+  p.tile_ctr = nullptr;
   p.total_tiles = static_cast<int>(tiles);
   p.n_mblocks = plan.n_mblocks;
   p.pair_heads = plan.pair;
@@ -651,14 +658,17 @@ int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* l
     if ((st = plan_buffer(dev, cs, B, &pb)) != ATTN_OK) return st;
     int* order = pb.ptr;
     int* start = order + pb.cap;
-    if (launch_fwd_plan(seqlens, B, N_q, H_q, p.pair_heads, order, start, err, cs) != cudaSuccess)
+    int* ctr = start + pb.cap + 1;
+    if (launch_fwd_plan(seqlens, B, N_q, H_q, p.pair_heads, order, start, ctr, err, cs) !=
+        cudaSuccess)
       return ATTN_ERR_CUDA;
     p.seq_order = order;
     p.tile_start = start;
     p.n_mblocks = 0;  // per sequence
+    if (plan.mode == kFwdClaimed) p.tile_ctr = ctr;
   }
   long long grid_x = tiles;
-  if (plan.mode == kFwdStriding) {
+  if (plan.mode == kFwdStriding || plan.mode == kFwdClaimed) {
     grid_x = plan.grid;
   } else if (plan.mode == kFwdBalancedList) {
     const int* sch = fwd_schedule(dev, cs, B, H_q, N_q, N_k, causal != 0, p.sec_heads,

@@ -52,6 +52,7 @@ struct FwdParams {
   // Work list of the forward (longest-processing-time-first order).
   const int* tile_list;   // balanced schedule: work tiles of CTA c are
   const int* cta_start;   //   tile_list[cta_start[c] .. cta_start[c + 1]) (nullptr: striding)
+  int* tile_ctr;          // claimed schedule: claim counter, zero at launch (nullptr: static)
   const int* seq_order;   // packed: virtual -> actual sequence, longest first
   const int* tile_start;  // packed: first work tile of each virtual sequence, [B + 1]
   int total_tiles;        // fixed length: B * n_mblocks * (H_q >> pair_heads)

@@ -96,7 +96,7 @@ struct FwdCfg {
 };
 
 // Work decode: one work tile = two 128-row query tiles of one (batch, query head).
-struct FwdTile {
+struct __align__(16) FwdTile {
   int b, h, h_kv;  // b < 0 marks the end of the work list
   int q0;          // first query row of tile 0, relative to the sequence
   int row_base;    // global packed-row offset of the sequence (0 for fixed length)
@@ -115,6 +115,11 @@ struct FwdWork {
   int L;         // sequence length (fixed length: N_q)
 };
 
+// Slots of the ring through which the scheduler warp hands the decoded work
+// tiles to the other roles, and the readers of each slot (the producer
+// thread, the MMA warp and the eight softmax warps).
+constexpr int kSchedSlots = 2;
+constexpr int kSchedReaders = 10;
 struct FwdBars {
   uint64_t q_full, q_empty;
   uint64_t s_full[2];
@@ -124,6 +129,11 @@ struct FwdBars {
   uint64_t s_free[2];    // separate P: the softmax has S_t in registers
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
+  // work tiles handed out by the scheduler warp
+  uint64_t sched_full[kSchedSlots];
+  uint64_t sched_empty[kSchedSlots];
+  int sched_taken;     // work tiles the producer has taken so far
+  FwdTile sched_t[kSchedSlots];
   uint32_t tmem_base;
 };
 // Longest-processing-time-first order of the work list (FlashAttention-4
@@ -199,7 +209,8 @@ __device__ __forceinline__ void expand_fwd_work(const FwdParams& p, const FwdWor
   }
 }
 
-// The k-th work tile of this CTA; false past the end of the list.
+// The k-th work tile of this CTA under a static schedule (balanced lists or
+// striding); false past the end of its share.
 __device__ __forceinline__ bool next_tile(const FwdParams& p, int k, FwdTile& t) {
   int v;
   if (p.tile_list) {
@@ -215,7 +226,36 @@ __device__ __forceinline__ bool next_tile(const FwdParams& p, int k, FwdTile& t)
   return true;
 }
 
-template <int DQK, int DV, int EMU>
+// The k-th work tile of this CTA under a claimed schedule, as the scheduler
+// warp published it; false past the end of the work list. `warp_reader` makes lane 0 release the slot
+// for the whole warp once every lane has read it (a single-thread reader
+// releases it itself). A wait that runs out sets `ok` to false.
+__device__ __forceinline__ bool read_tile(FwdBars* bars, int k, FwdTile& t, long long lim,
+                                          bool warp_reader, bool& ok) {
+  const int slot = k % kSchedSlots;
+  if (!mbar_wait(smem_addr(&bars->sched_full[slot]), (k / kSchedSlots) & 1, lim)) {
+    ok = false;
+    return false;
+  }
+  const int4* src = reinterpret_cast<const int4*>(&bars->sched_t[slot]);
+  int4* dst = reinterpret_cast<int4*>(&t);
+#pragma unroll
+  for (int w = 0; w < static_cast<int>(sizeof(FwdTile) / 16); ++w) dst[w] = src[w];
+  if (warp_reader) {
+    // lane 0's copy, broadcast, so the compiler knows every field is the same
+    // in all lanes (warp-uniform loop bounds and addresses)
+    int* f = reinterpret_cast<int*>(&t);
+#pragma unroll
+    for (int w = 0; w < static_cast<int>(sizeof(FwdTile) / 4); ++w)
+      f[w] = __shfl_sync(0xffffffffu, f[w], 0);
+    if ((threadIdx.x & 31) == 0) mbar_arrive(smem_addr(&bars->sched_empty[slot]));
+  } else {
+    mbar_arrive(smem_addr(&bars->sched_empty[slot]));
+  }
+  return t.b >= 0;
+}
+
+template <int DQK, int DV, int EMU, bool CLAIMED>
 __global__ void __launch_bounds__(384, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -245,6 +285,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(smem_addr(&bars->kv_full[i]), 1);
       mbar_init(smem_addr(&bars->kv_empty[i]), 1);
     }
+    if constexpr (CLAIMED) {
+      for (int i = 0; i < kSchedSlots; ++i) {
+        mbar_init(smem_addr(&bars->sched_full[i]), 1);
+        mbar_init(smem_addr(&bars->sched_empty[i]), kSchedReaders);
+      }
+    }
+    if constexpr (CLAIMED) bars->sched_taken = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -276,7 +323,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       int qk = 0;        // tiles whose Q was loaded (tiles that see no key load nothing)
       FwdTile t;
       bool ok = true;
-      for (int k = 0; ok && next_tile(p, k, t); ++k) {
+      for (int k = 0; ok && (CLAIMED ? read_tile(bars, k, t, lim, false, ok) : next_tile(p, k, t)); ++k) {
+        if constexpr (CLAIMED) *reinterpret_cast<volatile int*>(&bars->sched_taken) = k + 1;
         const int n_kv = max(t.n[0], t.n[1]);
         if (n_kv > 0) {
           // Q of this tile goes into the buffer once the previous tile's last
@@ -340,6 +388,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         }
       }
+      if (!ok) record_error(p.err, kErrTimeout);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -459,7 +508,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           ++ns[i];
           return true;
         };
-        for (int k = 0; ok && next_tile(p, k, t); ++k) {
+        for (int k = 0; ok && (CLAIMED ? read_tile(bars, k, t, lim, true, ok) : next_tile(p, k, t)); ++k) {
           const int n_kv = max(t.n[0], t.n[1]);
           if (n_kv == 0) continue;  // no keys: the epilogue writes O = 0, LSE = -inf
           ok = mbar_wait_warp(smem_addr(&bars->q_full), qk & 1, lim);
@@ -510,7 +559,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           ld += 2 * n_kv;
         }
       } else
-      for (int k = 0; ok && next_tile(p, k, t); ++k) {
+      for (int k = 0; ok && (CLAIMED ? read_tile(bars, k, t, lim, true, ok) : next_tile(p, k, t)); ++k) {
         const int n_kv = max(t.n[0], t.n[1]);
         if (n_kv == 0) continue;  // no keys: the epilogue writes O = 0, LSE = -inf
         ok = mbar_wait_warp(smem_addr(&bars->q_full), qk & 1, lim);
@@ -577,6 +626,94 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       if (!ok && leader) record_error(p.err, kErrTimeout);
     }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------- scheduler
+    // Claimed schedule (CLAIMED, tile_ctr set): the CTA starts with work tile
+    // blockIdx.x and claims every further one from a counter in global memory
+    // (zeroed before the launch), so CTAs that finish early take more tiles:
+    // greedy list scheduling over the longest-first work list. This warp
+    // decodes each claimed tile and hands it to the other roles through a ring
+    // of kSchedSlots slots. Under a static schedule the warp is idle and every
+    // role decodes its tiles itself.
+    if (CLAIMED && lane == 0) {
+      const int total = p.cu_seqlens ? p.tile_start[p.B] : p.total_tiles;
+      // the sequence of the last decoded tile, kept: consecutive claims of a
+      // CTA mostly fall in the same sequence
+      int c_t0 = 1, c_t1 = 0;  // its tile range [c_t0, c_t1) (empty: none kept)
+      FwdWork c_w;
+      c_w.b = 0; c_w.row_base = 0; c_w.L = 0; c_w.local = 0;
+      auto locate = [&](int v) {
+        if (p.cu_seqlens == nullptr) return locate_fwd_work(p, v);
+        if (v < c_t0 || v >= c_t1) {
+          // largest virtual sequence whose first tile is <= v
+          int lo = 0, hi = p.B;
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.tile_start[mid] <= v) lo = mid; else hi = mid;
+          }
+          c_t0 = p.tile_start[lo];
+          c_t1 = p.tile_start[lo + 1];
+          c_w.b = p.seq_order[lo];
+          const SeqSpan sp = seq_span(p.cu_seqlens, c_w.b, p.N_q, 0);
+          c_w.row_base = sp.start;
+          c_w.L = sp.len;
+        }
+        FwdWork w = c_w;
+        w.local = v - c_t0;
+        return w;
+      };
+      // Far from the end of the work list the next tile is claimed as soon as
+      // the last one is handed out, so the other roles never wait for a
+      // claim. In the last kNearRounds rounds a tile is claimed only once the
+      // producer has taken the one before, so no CTA holds large claimed tiles
+      // while others run out of work.
+      constexpr unsigned kNearRounds = 4;
+      bool near_end = false;
+      auto claim = [&](int k) {
+        unsigned u = blockIdx.x;
+        if (k > 0) {
+          const unsigned c = atomicAdd(reinterpret_cast<unsigned*>(p.tile_ctr), 1u);
+          u = c >= static_cast<unsigned>(total) ? total : gridDim.x + c;
+        }
+        near_end = u + kNearRounds * gridDim.x >= static_cast<unsigned>(total);
+        FwdTile t;
+        if (u < static_cast<unsigned>(total)) {
+          expand_fwd_work(p, locate(static_cast<int>(u)), t);
+        } else {
+          t = FwdTile{};
+          t.b = -1;
+        }
+        return t;
+      };
+      FwdTile t = claim(0);
+      for (int k = 0;; ++k) {
+        const int slot = k % kSchedSlots;
+        if (k >= kSchedSlots && !mbar_wait_sleep(smem_addr(&bars->sched_empty[slot]),
+                                                 ((k / kSchedSlots) - 1) & 1, lim, 200)) {
+          record_error(p.err, kErrTimeout);
+          break;
+        }
+        bars->sched_t[slot] = t;
+        mbar_arrive(smem_addr(&bars->sched_full[slot]));
+        if (t.b < 0) break;
+        if (near_end) {
+          // the producer has taken tile k (a plain counter it raises; no data
+          // depends on it)
+          bool taken = *reinterpret_cast<volatile int*>(&bars->sched_taken) > k;
+          const long long t0 = clock64();
+          while (!taken) {
+            if (clock64() - t0 > lim) break;
+            __nanosleep(100);
+            taken = *reinterpret_cast<volatile int*>(&bars->sched_taken) > k;
+          }
+          if (!taken) {  // the other roles' bounded waits end the CTA
+            record_error(p.err, kErrTimeout);
+            break;
+          }
+        }
+        t = claim(k + 1);
+      }
+    }
   }
     __syncwarp();
   } else {
@@ -595,7 +732,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     bool ok = true;
     for (int k = 0; ok; ++k) {
       FwdTile t;
-      if (!next_tile(p, k, t)) break;
+      if (!(CLAIMED ? read_tile(bars, k, t, lim, true, ok) : next_tile(p, k, t))) break;
       const int my_n = i ? t.n[1] : t.n[0];
       const int Lk = t.Lk;
       const int q0i = qtile_row(p, t, i);  // first row of this warpgroup's query tile
@@ -755,12 +892,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 // sort == 0 the input order is kept.
 __global__ void __launch_bounds__(1024)
 fwd_plan_kernel(const int* __restrict__ cu_seqlens, int B, int T, int H_q, int pair_heads, int sort,
-                int* seq_order, int* tile_start, int* err) {
+                int* seq_order, int* tile_start, int* tile_ctr, int* err) {
   extern __shared__ int plan_smem[];
   int* len = plan_smem;        // [B] when sorting
   int* ord = plan_smem + B;    // [B] when sorting
   __shared__ int warp_sum[32];
   const int tid = threadIdx.x;
+  if (tid == 0 && tile_ctr != nullptr) *tile_ctr = 0;  // the forward's claim counter
   // the lengths are those the forward decodes (clamped into the T packed rows);
   // an inconsistent offset array is reported through the error word
   check_cu_seqlens(cu_seqlens, B, T, err, tid, blockDim.x);
@@ -821,12 +959,12 @@ fwd_plan_kernel(const int* __restrict__ cu_seqlens, int B, int T, int H_q, int p
 
 // ------------------------------------------------------------------ host side
 
-template <int DQK, int DV, int EMU>
-static cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk,
+template <int DQK, int DV, int EMU, bool CLAIMED>
+static cudaError_t launch_fwd_impl_sched(const CUtensorMap& tq, const CUtensorMap& tk,
                                    const CUtensorMap& tv, const FwdParams& p, dim3 grid,
                                    cudaStream_t stream) {
   using Cfg = FwdCfg<DQK, DV>;
-  auto kern = attn_fwd_kernel<DQK, DV, EMU>;
+  auto kern = attn_fwd_kernel<DQK, DV, EMU, CLAIMED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -836,6 +974,15 @@ static cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk,
   e = cudaGetLastError();
   prof_end(slot, stream);
   return e;
+}
+
+// A claimed schedule (tile_ctr set) runs the instance with the scheduler warp.
+template <int DQK, int DV, int EMU>
+static cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk,
+                                   const CUtensorMap& tv, const FwdParams& p, dim3 grid,
+                                   cudaStream_t stream) {
+  if (p.tile_ctr != nullptr) return launch_fwd_impl_sched<DQK, DV, EMU, true>(tq, tk, tv, p, grid, stream);
+  return launch_fwd_impl_sched<DQK, DV, EMU, false>(tq, tk, tv, p, grid, stream);
 }
 
 // Number of exponentials per 8 pairs routed to the FMA polynomial (d = 64 has
@@ -862,7 +1009,8 @@ cudaError_t launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUte
 constexpr int kPlanMaxSort = 8192;
 
 cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int T, int H_q, int pair_heads,
-                            int* seq_order, int* tile_start, int* err, cudaStream_t stream) {
+                            int* seq_order, int* tile_start, int* tile_ctr, int* err,
+                            cudaStream_t stream) {
   const int sort = (B <= kPlanMaxSort) ? 1 : 0;
   const size_t smem = sort ? static_cast<size_t>(2) * B * sizeof(int) : 0;
   cudaError_t e = cudaFuncSetAttribute(fwd_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -870,7 +1018,7 @@ cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int T, int H_q, int pa
   if (e != cudaSuccess) return e;
   const int slot = prof_begin(kKFwdPlan, stream);
   fwd_plan_kernel<<<1, 1024, smem, stream>>>(cu_seqlens, B, T, H_q, pair_heads, sort, seq_order,
-                                              tile_start, err);
+                                              tile_start, tile_ctr, err);
   e = cudaGetLastError();
   prof_end(slot, stream);
   return e;

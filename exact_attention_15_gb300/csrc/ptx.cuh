@@ -58,6 +58,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long lo
   }
   return true;
 }
+// The same bounded wait for a thread that is never on the critical path: it
+// sleeps about `ns` nanoseconds between polls, so its spinning takes no issue
+// slots from the warps that share its scheduler.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, long long limit,
+                                                unsigned ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit) return false;
+    __nanosleep(ns);
+  }
+  return true;
+}
 
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {

@@ -111,11 +111,15 @@ typedef enum {
  * longest first).
  *
  * Packed inputs: the call first launches a one-CTA planning kernel that orders
- * the sequences longest first. It writes into a library-owned device buffer
- * (cudaMalloc'd on the first packed call on each device and stream, kept until
- * the process exits; a later call with more sequences than the buffer holds
- * synchronises that stream once and reallocates it). Make the first packed call
- * on a stream outside stream capture.
+ * the sequences longest first and zeroes a tile counter. It writes into a
+ * library-owned device buffer (cudaMalloc'd on the first packed call on each
+ * device and stream, kept until the process exits; a later call with more
+ * sequences than the buffer holds synchronises that stream once and
+ * reallocates it). Make the first packed call on a stream outside stream
+ * capture. With more work tiles than SMs the forward then runs one CTA per SM,
+ * and each CTA claims its next work tile from that counter when it is ready
+ * for one, so the CTAs share unequal sequences evenly; which CTA computes a
+ * tile does not change its results.
  *
  * Fixed-length causal shapes with long work tiles run on a persistent grid whose
  * CTAs take their tiles from a balanced list built on the host. The first call
@@ -299,7 +303,10 @@ int attn_debug_stall(attn_stream_t stream);
  * For the shape of an attn_fwd_dims call (varlen != 0: packed inputs, B
  * sequences of N_q = N_k total rows) on a GPU with n_sm SMs, writes six entries
  *   info[0] mode: 0 one CTA per work tile, 1 persistent grid with CTA c taking
- *           tiles c, c + grid, ..., 2 persistent grid over balanced lists
+ *           tiles c, c + grid, ..., 2 persistent grid over balanced lists,
+ *           3 persistent grid whose CTA c takes tile c first and then claims
+ *           the next unclaimed tile of the work list from a counter each time
+ *           it is ready for one (packed inputs with more tiles than SMs)
  *   info[1] grid size
  *   info[2] work tiles (two 128-row query tiles each; an upper bound when
  *           packed)

@@ -54,9 +54,14 @@ def test_mode_choice_for_causal_and_packed_shapes():
     # long causal tiles: balanced lists; short ones: striding (saving start-ups wins)
     assert b.attn_debug_fwd_plan(4, 16, 16, 8192, 8192, 128, 128, True, False, 152)["mode"] == BALANCED
     assert b.attn_debug_fwd_plan(64, 16, 16, 1024, 1024, 64, 64, True, False, 152)["mode"] == STRIDING
-    # packed inputs never use host lists (their lengths live on the device)
+    # packed inputs never use host lists (their lengths live on the device):
+    # with more tiles than SMs, a persistent grid claims them from a counter
     for N in (4096, 40000, 300000):
-        assert b.attn_debug_fwd_plan(16, 32, 8, N, N, 128, 128, True, True, 152)["mode"] != BALANCED
+        p = b.attn_debug_fwd_plan(16, 32, 8, N, N, 128, 128, True, True, 152)
+        if p["tiles"] > 152:
+            assert (p["mode"], p["grid"]) == (b.FWD_CLAIMED, 152)
+        else:
+            assert (p["mode"], p["grid"]) == (ONE_CTA, p["tiles"])
     # L2 sections: K + V of 8 heads (4 MiB each at N = 8192, d = 128) fit the 48 MiB share
     assert b.attn_debug_fwd_plan(4, 16, 16, 8192, 8192, 128, 128, True, False, 152)["sec_heads"] == 8
 
