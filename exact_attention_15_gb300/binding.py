@@ -55,7 +55,8 @@ _SIGS = {
 
 KERNEL_NAMES = {1: "attn_fwd_kernel", 2: "attn_bwd_pre_kernel", 3: "attn_bwd_main_kernel",
                 4: "attn_bwd_post_kernel", 5: "exp2_probe_kernel", 6: "stall_probe_kernel",
-                7: "fwd_plan_kernel", 8: "attn_fwd_pair_kernel", 9: "attn_bwd_main_kernel_pass2"}
+                7: "fwd_plan_kernel", 8: "attn_fwd_pair_kernel", 9: "attn_bwd_main_kernel_pass2",
+                10: "bwd_plan_kernel"}
 FAULT_NONE = 0
 FAULT_SKIP_DQ_RELEASE = 1
 BWD_ONE_CTA = 0

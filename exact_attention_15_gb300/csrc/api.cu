@@ -28,6 +28,9 @@ cudaError_t launch_attn_fwd_pair(const CUtensorMap& tq, const CUtensorMap& tk_ha
 cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int T, int H_q, int pair_heads,
                             int* seq_order, int* tile_start, int* tile_ctr, int* err,
                             cudaStream_t stream);
+cudaError_t launch_seq_plan(const int* cu_seqlens, int B, int T, int rows, int units,
+                            int* seq_order, int* tile_start, int* tile_ctr, int* err, int prof_id,
+                            cudaStream_t stream);
 cudaError_t launch_exp2_probe(const float* x, float* y, int n, int mode, cudaStream_t stream);
 cudaError_t launch_stall_probe(int* err, long long limit, cudaStream_t stream);
 int read_rescale_stats(unsigned long long* out, int reset);
@@ -424,7 +427,7 @@ struct BwdPlan {
   long long rows_q;     // rows of the [rows, H_q, d] view of q
   long long slots;      // query-tile slots (deterministic semaphores), per head
   long long n_work;     // CTAs of the main kernel (upper bound for packed inputs)
-  size_t acc_off, dvec_off, sem_off, total;
+  size_t acc_off, dvec_off, sem_off, order_off, total;
 };
 
 bool fwd_uses_pairs() {
@@ -492,8 +495,10 @@ bool bwd_plan(int B, int H_q, int H_kv, int N_q, int N_k, int d, bool varlen, bo
   pl->acc_off = 0;
   pl->dvec_off = align256(static_cast<size_t>(pl->rows_q) * H_q * d * 4);
   pl->sem_off = pl->dvec_off + align256(static_cast<size_t>(pl->rows_q) * H_q * 4);
-  pl->total = pl->sem_off +
-              (det ? align256(static_cast<size_t>(pl->slots * H_q + 1) * passes * 4) : 0);
+  pl->order_off = pl->sem_off +
+                  (det ? align256(static_cast<size_t>(pl->slots * H_q + 1) * passes * 4) : 0);
+  // packed: the sequence order and the first work item of each sequence
+  pl->total = pl->order_off + (varlen ? align256((2 * static_cast<size_t>(B) + 1) * 4) : 0);
   return true;
 }
 
@@ -799,6 +804,20 @@ int attn_bwd_dims(const void* q, const void* k, const void* v, const void* o, co
   p.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
   p.fault = g_fault.load(std::memory_order_relaxed);
   p.pairs = pairs ? 1 : 0;
+  p.sem_slots = static_cast<int>(pl.slots);
+  p.seq_order = nullptr;
+  p.item_start = nullptr;
+  if (seqlens && !pairs) {
+    // packed: the work items walk the sequences longest first (greedy dispatch
+    // of unequal items then ends with the short ones)
+    int* order = reinterpret_cast<int*>(ws + pl.order_off);
+    int* start = order + B;
+    if (launch_seq_plan(seqlens, B, N_q, kTileN, H_kv, order, start, nullptr, err, kKBwdPlan, cs) !=
+        cudaSuccess)
+      return ATTN_ERR_CUDA;
+    p.seq_order = order;
+    p.item_start = start;
+  }
   // Deterministic order of the dQ additions: under a causal mask, and without
   // one when queries and keys have equal lengths and the key tiles of a (batch,
   // KV head) are few (non-causal key tiles wait on one another in a cycle, so

@@ -102,6 +102,33 @@ __device__ __forceinline__ bool decode_bwd_tile(const BwdParams& p, int idx, Bwd
     t.Lq = p.N_q;
     t.Lk = p.N_k;
     t.sem_base = t.b * ((p.N_q + kTileM - 1) / kTileM);
+  } else if (p.seq_order != nullptr) {
+    // sequences longest first; inside one, key tile major (every KV head of key
+    // tile j before key tile j + 1), which deals the long items out first
+    if (idx >= __ldg(p.item_start + p.B)) return false;
+    int lo = 0, hi = p.B;  // largest virtual sequence whose first item is <= idx
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.item_start + mid) <= idx) lo = mid; else hi = mid;
+    }
+    const int first = __ldg(p.item_start + lo);
+    const SeqSpan sp = seq_span(p.cu_seqlens, __ldg(p.seq_order + lo), p.N_q, 0);
+    const int L = sp.len;
+    const int nk = (L + kTileN - 1) / kTileN;
+    const int local = idx - first;
+    const int jj = local / p.H_kv;
+    t.j = SPT ? nk - 1 - jj : jj;
+    t.h_kv = local - jj * p.H_kv;
+    t.b = __ldg(p.seq_order + lo);
+    t.row_base = sp.start;
+    t.batch_coord = 0;
+    t.Lq = L;
+    t.Lk = L;
+    // a sequence's query tiles take the slots after those of the sequences
+    // before it in this order; an inconsistent offset array (reported by the
+    // planning kernel) could run them past the semaphore array
+    t.sem_base = first / p.H_kv;
+    if (t.sem_base + (L + kTileM - 1) / kTileM > p.sem_slots) return false;
   } else {
     // sequences in order, each clamped after the one before it (seq_span), so
     // their query-tile slots stay within the semaphore array

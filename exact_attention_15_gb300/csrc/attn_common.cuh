@@ -79,12 +79,19 @@ struct BwdParams {
   int pairs;            // d = 128: run the CTA-pair main kernel
   int spt;              // deterministic one-CTA kernel: key tiles in descending order,
                         // query tiles walked from the key tile's own, dQ added in step order
+  // packed inputs, one-CTA kernels: the work items walk the sequences longest
+  // first (seq_order: virtual -> actual sequence; item_start[v]: first item of
+  // virtual sequence v, B + 1 entries); nullptr: input order
+  const int* seq_order;
+  const int* item_start;
+  int sem_slots;        // query-tile slots per head the semaphore array holds
 };
 
 // Kernel tracing (host side, implemented next to the C ABI). prof_begin
 // returns a slot (or -1 when tracing is off); prof_end closes it.
 enum KernelId : int { kKFwd = 1, kKBwdPre = 2, kKBwdMain = 3, kKBwdPost = 4, kKExp2 = 5,
-                      kKStall = 6, kKFwdPlan = 7, kKFwdPair = 8, kKBwdMain2 = 9 };
+                      kKStall = 6, kKFwdPlan = 7, kKFwdPair = 8, kKBwdMain2 = 9,
+                      kKBwdPlan = 10 };
 int prof_begin(int kernel, cudaStream_t stream);
 void prof_end(int slot, cudaStream_t stream);
 

@@ -884,14 +884,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   }
 }
 
-// Orders packed sequences longest first (their longest work tile is the
-// longest) and writes the forward's work-list metadata: seq_order maps a
-// virtual sequence index to the actual one and tile_start[v] is the first work
-// tile of virtual sequence v (FlashAttention-4 summary, section 3.3, the
-// varlen scheduling paragraph). One CTA. Ties keep their input order; with
-// sort == 0 the input order is kept.
+// Orders packed sequences longest first (their longest work item is the
+// longest) and writes a work list's metadata: seq_order maps a virtual
+// sequence index to the actual one and tile_start[v] is the first work item of
+// virtual sequence v, a sequence of L rows having ceil(L / rows) * units items
+// (FlashAttention-4 summary, section 3.3, the varlen scheduling paragraph).
+// The forward's items are its work tiles, the backward's its (key tile, KV
+// head) items. One CTA. Ties keep their input order; with sort == 0 the input
+// order is kept.
 __global__ void __launch_bounds__(1024)
-fwd_plan_kernel(const int* __restrict__ cu_seqlens, int B, int T, int H_q, int pair_heads, int sort,
+seq_plan_kernel(const int* __restrict__ cu_seqlens, int B, int T, int rows, int units, int sort,
                 int* seq_order, int* tile_start, int* tile_ctr, int* err) {
   extern __shared__ int plan_smem[];
   int* len = plan_smem;        // [B] when sorting
@@ -899,7 +901,7 @@ fwd_plan_kernel(const int* __restrict__ cu_seqlens, int B, int T, int H_q, int p
   __shared__ int warp_sum[32];
   const int tid = threadIdx.x;
   if (tid == 0 && tile_ctr != nullptr) *tile_ctr = 0;  // the forward's claim counter
-  // the lengths are those the forward decodes (clamped into the T packed rows);
+  // the lengths are those the kernels decode (clamped into the T packed rows);
   // an inconsistent offset array is reported through the error word
   check_cu_seqlens(cu_seqlens, B, T, err, tid, blockDim.x);
   if (sort) {
@@ -923,8 +925,7 @@ fwd_plan_kernel(const int* __restrict__ cu_seqlens, int B, int T, int H_q, int p
   auto tiles_of = [&](int vs) {
     const int s = sort ? ord[vs] : vs;
     const int L = sort ? len[s] : seq_span(cu_seqlens, s, T, 0).len;
-    const int mrows = (2 * kTileM) >> pair_heads;
-    return (L + mrows - 1) / mrows * (H_q >> pair_heads);
+    return (L + rows - 1) / rows * units;
   };
   int local = 0;
   for (int vs = v0; vs < v1; ++vs) local += tiles_of(vs);
@@ -1008,20 +1009,27 @@ cudaError_t launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUte
 // shared memory); larger batches keep their input order.
 constexpr int kPlanMaxSort = 8192;
 
-cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int T, int H_q, int pair_heads,
-                            int* seq_order, int* tile_start, int* tile_ctr, int* err,
+cudaError_t launch_seq_plan(const int* cu_seqlens, int B, int T, int rows, int units,
+                            int* seq_order, int* tile_start, int* tile_ctr, int* err, int prof_id,
                             cudaStream_t stream) {
   const int sort = (B <= kPlanMaxSort) ? 1 : 0;
   const size_t smem = sort ? static_cast<size_t>(2) * B * sizeof(int) : 0;
-  cudaError_t e = cudaFuncSetAttribute(fwd_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(seq_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        2 * kPlanMaxSort * static_cast<int>(sizeof(int)));
   if (e != cudaSuccess) return e;
-  const int slot = prof_begin(kKFwdPlan, stream);
-  fwd_plan_kernel<<<1, 1024, smem, stream>>>(cu_seqlens, B, T, H_q, pair_heads, sort, seq_order,
+  const int slot = prof_begin(prof_id, stream);
+  seq_plan_kernel<<<1, 1024, smem, stream>>>(cu_seqlens, B, T, rows, units, sort, seq_order,
                                               tile_start, tile_ctr, err);
   e = cudaGetLastError();
   prof_end(slot, stream);
   return e;
+}
+
+cudaError_t launch_fwd_plan(const int* cu_seqlens, int B, int T, int H_q, int pair_heads,
+                            int* seq_order, int* tile_start, int* tile_ctr, int* err,
+                            cudaStream_t stream) {
+  return launch_seq_plan(cu_seqlens, B, T, (2 * kTileM) >> pair_heads, H_q >> pair_heads,
+                         seq_order, tile_start, tile_ctr, err, kKFwdPlan, stream);
 }
 
 // Reads (and with reset clears) the rescale counters; returns the number of

@@ -155,8 +155,9 @@ int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* l
  * sizes). Arguments mean what they mean for attn_bwd; `varlen` is non-zero when
  * attn_bwd will be given a cu_seqlens array (then N_q is the packed row count).
  * The workspace holds the fp32 dQ accumulator [rows, H_q, d], D = rowsum(dO o O)
- * (laid out like lse) and, in deterministic mode, one ordering semaphore per
- * (query tile, query head) plus a work counter.
+ * (laid out like lse), in deterministic mode one ordering semaphore per
+ * (query tile, query head) plus a work counter, and for packed inputs the
+ * order in which the backward walks the sequences (2 B + 1 ints).
  */
 size_t attn_bwd_workspace_bytes(int B, int H_q, int H_kv, int N_q, int N_k, int d, int varlen,
                                 int deterministic);
@@ -379,7 +380,8 @@ long long attn_set_wait_limit(long long cycles);
  * Kernel ids: 1 forward, 2 backward pre (D, zeroing), 3 backward main (its first
  * pass at d_qk = 192), 4 backward post (dQ conversion), 5 exp2 test hook, 6 stall
  * test hook, 7 forward planning kernel (packed inputs), 8 forward on CTA pairs
- * (ATTN_FWD_CTA_PAIR), 9 second pass of the backward main kernel (d_qk = 192).
+ * (ATTN_FWD_CTA_PAIR), 9 second pass of the backward main kernel (d_qk = 192),
+ * 10 backward planning kernel (packed inputs).
  */
 typedef struct {
   int kernel;  /* kernel id, see above */

@@ -127,9 +127,11 @@ def test_workspace_size(lib):
     assert lib.attn_bwd_workspace_bytes(B, H, H, N, N, d, 0, 0) == acc + dvec
     sem = B * (N // 128) * H + 1
     assert lib.attn_bwd_workspace_bytes(B, H, H, N, N, d, 0, 1) == acc + dvec + ((sem * 4 + 255) // 256) * 256
-    # packed: rows = N_q (the packed total), not B * N_q
+    # packed: rows = N_q (the packed total), not B * N_q, and the sequence
+    # order (B ints) with each sequence's first work item (B + 1 ints)
     assert lib.attn_bwd_workspace_bytes(16, 32, 8, 1000, 1000, 128, 1, 0) == \
-        ((1000 * 32 * 128 * 4 + 255) // 256) * 256 + ((1000 * 32 * 4 + 255) // 256) * 256
+        ((1000 * 32 * 128 * 4 + 255) // 256) * 256 + ((1000 * 32 * 4 + 255) // 256) * 256 + \
+        (((2 * 16 + 1) * 4 + 255) // 256) * 256
     assert lib.attn_bwd_workspace_bytes(1, 2, 2, 10, 10, 96, 0, 0) == 0
 
 

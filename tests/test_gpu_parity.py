@@ -208,6 +208,65 @@ def test_balanced_schedule_writes_every_tile(B, H, N, d, H_kv):
     _oracle_fwd_check(inp, outs[0][0], outs[0][1], pairs, rows)
 
 
+@pytest.mark.parametrize("d,causal,H_q,H_kv", [(128, True, 4, 1), (128, False, 2, 2), (64, True, 4, 2),
+                                               (192, True, 2, 1)])
+def test_claimed_schedule_packed(d, causal, H_q, H_kv):
+    """Packed inputs with more work tiles than SMs run on a persistent grid whose
+    CTAs claim tiles from a device counter (zeroed by the planning kernel at every
+    call). Every row must be written (outputs start as NaN), repeated calls and a
+    CUDA-graph replay must give the same bits, and every (sequence, head) matches
+    the oracle. The lengths include empty and one-row sequences and several whole
+    and ragged tiles."""
+    import torch
+    from exact_attention_15_gb300 import binding
+    from gpu_common import device_inputs
+    rng = np.random.default_rng(900 + d)
+    lens = [int(x) for x in rng.integers(0, 700, size=56)] + [0, 1, 0, 128, 256, 1500, 2]
+    d_v = 128 if d == 192 else d
+    inp = W.custom(0, H_q, H_kv, 0, 0, d, causal=causal, seed=901 + d, seqlens=lens,
+                   parts=("q", "k", "v"), d_v=d_v)
+    T = inp.N_q
+    plan = binding.attn_debug_fwd_plan(len(lens), H_q, H_kv, T, T, d, d_v, causal, True, 152)
+    assert plan["mode"] == binding.FWD_CLAIMED and plan["tiles"] > 152
+    dev = device_inputs(inp)
+
+    def fwd(o, lse):
+        binding.forward(dev["q"], dev["k"], dev["v"], scale=inp.scale, causal=causal,
+                        cu_seqlens=dev["cu"], out=o, lse=lse)
+
+    outs = []
+    for _ in range(3):
+        o = torch.full((T, H_q, d_v), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((H_q, T), float("nan"), dtype=torch.float32, device="cuda")
+        fwd(o, lse)
+        torch.cuda.synchronize()
+        assert binding.attn_check(None) == 0
+        assert not torch.isnan(o).any().item(), "an output row was not written"
+        assert not torch.isnan(lse).any().item(), "an LSE row was not written"
+        outs.append((o, lse))
+    for o, lse in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0][0].view(torch.int16))
+        assert torch.equal(lse, outs[0][1])
+    go = torch.full((T, H_q, d_v), float("nan"), dtype=torch.bfloat16, device="cuda")
+    gl = torch.full((H_q, T), float("nan"), dtype=torch.float32, device="cuda")
+    # the first packed call on a stream (which sets up its planning buffer) is
+    # made outside capture, as the C ABI asks
+    cap = torch.cuda.Stream()
+    with torch.cuda.stream(cap):
+        fwd(go, gl)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        fwd(go, gl)
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        assert binding.attn_check(None) == 0
+        assert torch.equal(go.view(torch.int16), outs[0][0].view(torch.int16))
+        assert torch.equal(gl, outs[0][1])
+    _oracle_fwd_check(inp, outs[0][0], outs[0][1], _all_pairs(inp))
+
+
 def test_forward_on_concurrent_streams():
     """Forward passes issued on two streams at once give the same bits as the
     same passes run one after the other, launch after launch."""
