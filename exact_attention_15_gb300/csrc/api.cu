@@ -807,6 +807,22 @@ int attn_bwd_dims(const void* q, const void* k, const void* v, const void* o, co
   p.sem_slots = static_cast<int>(pl.slots);
   p.seq_order = nullptr;
   p.item_start = nullptr;
+  p.sec_heads = 0;
+  // only for long items (at least 32 key tiles a pair): the longest item is
+  // then a sizeable share of an SM's work, while with short items the pairs'
+  // shared Q, dO and dQ rows in L2 are worth more than the balance
+  if (causal && !seqlens && !pairs && (N_k + kTileN - 1) / kTileN >= 32) {
+    // (batch, KV head) pairs per section: as many as keep what their items
+    // stream within 48 MiB of L2: the GQA group's Q and dO (bf16, d_qk + d_v
+    // values a row) and its fp32 dQ accumulator (d_qk values a row)
+    constexpr long long kBudget = 48ll << 20;
+    const long long per_pair =
+        static_cast<long long>(N_q) * (H_q / H_kv) * (2ll * (d_qk + d_v) + 4ll * d_qk);
+    long long fit = per_pair > 0 ? kBudget / per_pair : 1;
+    if (fit < 1) fit = 1;
+    if (fit > static_cast<long long>(B) * H_kv) fit = static_cast<long long>(B) * H_kv;
+    p.sec_heads = static_cast<int>(fit);
+  }
   if (seqlens && !pairs) {
     // packed: the work items walk the sequences longest first (greedy dispatch
     // of unequal items then ends with the short ones)

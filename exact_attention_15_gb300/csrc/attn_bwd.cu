@@ -92,10 +92,26 @@ __device__ __forceinline__ bool decode_bwd_tile(const BwdParams& p, int idx, Bwd
   if (p.cu_seqlens == nullptr) {
     const int nk = (p.N_k + kTileN - 1) / kTileN;
     if (nk == 0) return false;
-    t.j = SPT ? nk - 1 - idx % nk : idx % nk;
-    const int rest = idx / nk;
-    t.h_kv = rest % p.H_kv;
-    t.b = rest / p.H_kv;
+    int jj, pair;  // key-tile step and (batch, KV head) pair of the item
+    if (p.sec_heads > 0) {
+      // causal: sections of sec_heads pairs whose Q and dO fit in L2; inside a
+      // section key tile major (every pair's key tile j before key tile j + 1),
+      // so the long items near the diagonal's start are dealt out first
+      const int per_sec = p.sec_heads * nk;
+      const int sec = idx / per_sec;
+      const int r = idx - sec * per_sec;
+      const int n_pairs = p.B * p.H_kv;
+      const int in_sec = min(p.sec_heads, n_pairs - sec * p.sec_heads);
+      if (in_sec <= 0) return false;
+      jj = r / in_sec;
+      pair = sec * p.sec_heads + (r - jj * in_sec);
+    } else {
+      jj = idx % nk;
+      pair = idx / nk;
+    }
+    t.j = SPT ? nk - 1 - jj : jj;
+    t.h_kv = pair % p.H_kv;
+    t.b = pair / p.H_kv;
     if (t.b >= p.B) return false;
     t.row_base = 0;
     t.batch_coord = t.b;

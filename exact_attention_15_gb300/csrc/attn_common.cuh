@@ -85,6 +85,8 @@ struct BwdParams {
   const int* seq_order;
   const int* item_start;
   int sem_slots;        // query-tile slots per head the semaphore array holds
+  int sec_heads;        // fixed length, causal: (batch, KV head) pairs per L2 section whose
+                        // items run key tile major; 0: each pair's key tiles in a row
 };
 
 // Kernel tracing (host side, implemented next to the C ABI). prof_begin
