@@ -844,20 +844,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             p.cu_seqlens ? (grow * p.H_q + hq) * DV
                          : ((static_cast<size_t>(t.b) * p.N_q + qrow) * p.H_q + hq) * DV;
         uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + o_off);
+        // the row's O columns are loaded with every load in flight at once (one
+        // wait instead of one per 32 columns), then scaled, rounded and stored
+        uint32_t ov[DV];
+        if (have_o) {
+#pragma unroll
+          for (int cc = 0; cc < DV / 32; ++cc)
+            tmem_ld32(tmem + lane_base + col_o + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(ov + cc * 32));
+#pragma unroll
+          for (int cc = 0; cc < DV / 32; ++cc) tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(ov + cc * 32));
+        } else {
+#pragma unroll
+          for (int e = 0; e < DV; ++e) ov[e] = 0u;
+        }
 #pragma unroll
         for (int cc = 0; cc < DV / 32; ++cc) {
-          uint32_t ov[32];
-          if (have_o) {
-            tmem_ld32(tmem + lane_base + col_o + cc * 32, ov);
-            tmem_ld_wait(ov);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = 0u;
-          }
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv_l, __uint_as_float(ov[2 * e + 1]) * inv_l);
+            w[e] = pack_bf16x2(__uint_as_float(ov[cc * 32 + 2 * e]) * inv_l,
+                               __uint_as_float(ov[cc * 32 + 2 * e + 1]) * inv_l);
           if (row_ok) {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
