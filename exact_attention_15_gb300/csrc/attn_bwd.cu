@@ -349,6 +349,30 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                         t.row_base + t.j * kTileN, t.batch_coord);
         }
         float* stat = reinterpret_cast<float*>(smem + Cfg::kStatOff);
+        // LSE (to log2 units) and D of the 128 rows of a query tile, four rows a
+        // lane; rows past the end get LSE = +inf so that their P is exactly 0.
+        // They are loaded one tile ahead, so the global loads' round trip
+        // overlaps the waits for the next Q stage and dO buffer instead of
+        // following them.
+        float lv[4], dv[4];
+        auto load_stats = [&](int it) {
+          const int h = t.h_kv * p.group + it / n_per_head;
+          const int i = bwd_query_tile<SPT>(p, t, it % n_per_head);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int q = i * kTileM + lane + 32 * e;
+            lv[e] = INFINITY;
+            dv[e] = 0.f;
+            if (q < t.Lq) {
+              const size_t off = p.cu_seqlens
+                                     ? static_cast<size_t>(h) * p.N_q + t.row_base + q
+                                     : (static_cast<size_t>(t.b) * p.H_q + h) * p.N_q + q;
+              lv[e] = p.lse[off];
+              dv[e] = p.dvec[off];
+            }
+          }
+        };
+        load_stats(0);
         for (int it = 0; it < n_it; ++it) {
           const int stage = it % kQS;
           const int h = t.h_kv * p.group + it / n_per_head;
@@ -364,27 +388,17 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
               tma_load_4d(smem_addr(smem + Cfg::kQOff + stage * Cfg::kQKBytes) + hf * 16384, &tm_q,
                           fb, hf * 64, h, t.row_base + i * kTileM, t.batch_coord);
           }
-          // LSE (to log2 units) and D for the 128 rows of this query tile; rows
-          // past the end get LSE = +inf so that their P is exactly 0.
           float* lse2 = stat + stage * 256;
           float* dvs = lse2 + 128;
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int r = lane + 32 * e;
-            const int q = i * kTileM + r;
-            float lv = INFINITY, dv = 0.f;
-            if (q < t.Lq) {
-              const size_t off = p.cu_seqlens
-                                     ? static_cast<size_t>(h) * p.N_q + t.row_base + q
-                                     : (static_cast<size_t>(t.b) * p.H_q + h) * p.N_q + q;
-              lv = p.lse[off] * kLog2e;
-              dv = p.dvec[off];
-              if (lv == -INFINITY) lv = INFINITY;  // a row that saw no key has no gradient
-            }
-            lse2[r] = lv;
-            dvs[r] = dv;
+            float l2 = lv[e] * kLog2e;
+            if (l2 == -INFINITY) l2 = INFINITY;  // a row that saw no key has no gradient
+            lse2[lane + 32 * e] = l2;
+            dvs[lane + 32 * e] = dv[e];
           }
           mbar_arrive(fb);
+          if (it + 1 < n_it) load_stats(it + 1);
           // dO_i into the single dO buffer once dV_{i-1} has read it
           if (!mbar_wait(smem_addr(&bars->do_empty), (it & 1) ^ 1, lim)) {
             record_error(p.err, kErrTimeout);
