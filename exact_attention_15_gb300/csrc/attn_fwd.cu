@@ -233,7 +233,11 @@ __device__ __forceinline__ bool next_tile(const FwdParams& p, int k, FwdTile& t)
 __device__ __forceinline__ bool read_tile(FwdBars* bars, int k, FwdTile& t, long long lim,
                                           bool warp_reader, bool& ok) {
   const int slot = k % kSchedSlots;
-  if (!mbar_wait(smem_addr(&bars->sched_full[slot]), (k / kSchedSlots) & 1, lim)) {
+  // a warp decides together (the broadcast below needs every lane), even when
+  // the wait runs out
+  const uint32_t full = smem_addr(&bars->sched_full[slot]);
+  const uint32_t parity = (k / kSchedSlots) & 1;
+  if (!(warp_reader ? mbar_wait_warp(full, parity, lim) : mbar_wait(full, parity, lim))) {
     ok = false;
     return false;
   }
