@@ -20,8 +20,8 @@
 
 namespace attn {
 cudaError_t launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const FwdParams& p, dim3 grid,
-                            cudaStream_t stream);
+                            const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& p,
+                            dim3 grid, cudaStream_t stream);
 cudaError_t launch_attn_fwd_pair(const CUtensorMap& tq, const CUtensorMap& tk_half,
                                  const CUtensorMap& tv, const FwdParams& p, dim3 grid,
                                  cudaStream_t stream);
@@ -618,10 +618,11 @@ int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* l
   int* err = nullptr;
   if ((st = device_setup(dev, &err)) != ATTN_OK) return st;
 
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   // with no keys at all nothing is ever loaded from k/v; map q instead of an empty extent
   const bool no_keys = (N_k == 0);
   if (encode_rows_map(&tq, q, d_qk, H_q, s.q_rows, s.q_batch) != ATTN_OK ||
+      encode_rows_map(&to, o, d_v, H_q, s.q_rows, s.q_batch) != ATTN_OK ||
       encode_rows_map(&tk, no_keys ? q : k, d_qk, no_keys ? H_q : H_kv,
                       no_keys ? s.q_rows : s.k_rows, s.q_batch) != ATTN_OK ||
       encode_rows_map(&tv, no_keys ? q : v, d_v, no_keys ? H_q : H_kv,
@@ -684,7 +685,7 @@ int attn_fwd_dims(const void* q, const void* k, const void* v, void* o, float* l
       grid_x = plan.grid;
     }
   }
-  if (launch_attn_fwd(d_qk, d_v, tq, tk, tv, p, dim3(static_cast<unsigned>(grid_x)), cs) !=
+  if (launch_attn_fwd(d_qk, d_v, tq, tk, tv, to, p, dim3(static_cast<unsigned>(grid_x)), cs) !=
       cudaSuccess)
     return ATTN_ERR_CUDA;
   return ATTN_OK;

@@ -82,7 +82,14 @@ struct FwdCfg {
   static constexpr int kKVOff = 2 * kQTileBytes;
   static constexpr int kRingBytes = kBlockRing ? kSlots * kBlockBytes : kStages * kTileBytes;
   static constexpr int kBarOff = kKVOff + kRingBytes;
+  // Equal head dimensions leave room for one 16 KB staging buffer per softmax
+  // warpgroup: O can leave through shared memory and TMA stores (whole 128-byte
+  // rows) instead of each thread storing its own row (kernels that use it ask
+  // for kSmemBytesEpi).
+  static constexpr bool kTmaEpi = DQK == DV;
+  static constexpr int kOEpiOff = kBarOff + 1024;  // 1024-aligned for the 128-byte swizzle
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // barriers + alignment slack
+  static constexpr int kSmemBytesEpi = kTmaEpi ? kOEpiOff + 2 * kBlockBytes + 1024 : kSmemBytes;
   static constexpr uint32_t kColO0 = 0, kColO1 = DV;
   static constexpr uint32_t kColS0 = 2 * DV, kColS1 = 2 * DV + 128;
   // d = 64: O (64 columns each) leaves room for P in its own columns (bf16
@@ -92,7 +99,8 @@ struct FwdCfg {
   static constexpr uint32_t kColP0 = kSepP ? 2 * DV + 256 : kColS0;
   static constexpr uint32_t kColPStep = kSepP ? 64 : 128;  // P_1 = P_0 + kColPStep
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert(kSmemBytes <= 232448 && kSmemBytesEpi <= 232448, "shared memory");
+  static_assert(kOEpiOff % 1024 == 0, "staging buffer alignment");
 };
 
 // Work decode: one work tile = two 128-row query tiles of one (batch, query head).
@@ -262,8 +270,13 @@ __device__ __forceinline__ bool read_tile(FwdBars* bars, int k, FwdTile& t, long
 template <int DQK, int DV, int EMU, bool CLAIMED>
 __global__ void __launch_bounds__(384, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                const FwdParams p) {
   using Cfg = FwdCfg<DQK, DV>;
+  // The staged O epilogue pays at d = 64 and for packed inputs (short work
+  // tiles, where the epilogue weighs most); with d = 128 and fixed lengths the
+  // tiles are long and direct row stores measured faster.
+  constexpr bool kTmaEpiUsed = Cfg::kTmaEpi && (DQK == 64 || CLAIMED);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -850,6 +863,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + o_off);
         // the row's O columns are loaded with every load in flight at once (one
         // wait instead of one per 32 columns), then scaled, rounded and stored
+        // (the last tile of a packed sequence row by row: a 128-row box would
+        // also write the next sequence's rows)
+        const bool tma_epi = kTmaEpiUsed && (p.cu_seqlens == nullptr || q0i + kTileM <= t.Lq);
         uint32_t ov[DV];
         if (have_o) {
 #pragma unroll
@@ -861,17 +877,46 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
           for (int e = 0; e < DV; ++e) ov[e] = 0u;
         }
+        if (tma_epi) {
+          // 64 columns at a time into this warpgroup's swizzled staging buffer,
+          // then one TMA store of the 128 x 64 box; the buffer is refilled once
+          // the previous store has read it
+          uint32_t buf_off = Cfg::kOEpiOff + i * Cfg::kBlockBytes;
+          asm volatile("" : "+r"(buf_off));  // computed here, not kept across the key loop
+          uint8_t* buf = smem + buf_off;
 #pragma unroll
-        for (int cc = 0; cc < DV / 32; ++cc) {
-          uint32_t w[16];
+          for (int hf = 0; hf < DV / 64; ++hf) {
+            uint32_t w[32];  // scaled and rounded before the wait, so the fp32 values can go
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(ov[cc * 32 + 2 * e]) * inv_l,
-                               __uint_as_float(ov[cc * 32 + 2 * e + 1]) * inv_l);
-          if (row_ok) {
+            for (int e = 0; e < 32; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(ov[hf * 64 + 2 * e]) * inv_l,
+                                 __uint_as_float(ov[hf * 64 + 2 * e + 1]) * inv_l);
+            if (r == 0) bulk_wait_group_read<0>();
+            named_bar_sync(2 + i, 128);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              orow[cc * 4 + e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            for (int ch = 0; ch < 8; ++ch)
+              *reinterpret_cast<uint4*>(buf + sw128_offset(r, ch)) =
+                  make_uint4(w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
+            fence_async_shared();
+            named_bar_sync(2 + i, 128);
+            if (r == 0) {
+              tma_store_4d(&tm_o, smem_addr(buf), hf * 64, hq, t.row_base + q0i, t.batch_coord);
+              bulk_commit_group();
+            }
+          }
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < DV / 32; ++cc) {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(ov[cc * 32 + 2 * e]) * inv_l,
+                                 __uint_as_float(ov[cc * 32 + 2 * e + 1]) * inv_l);
+            if (row_ok) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                orow[cc * 4 + e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            }
           }
         }
         if (row_ok) {
@@ -884,6 +929,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       pvc += my_n;
     }
+    // the O stores have read the staging buffer before the CTA's shared memory goes
+    if (kTmaEpiUsed && r == 0) bulk_wait_group<0>();
     if (!ok) record_error(p.err, kErrTimeout);
   }
   tc_fence_before();
@@ -972,16 +1019,16 @@ seq_plan_kernel(const int* __restrict__ cu_seqlens, int B, int T, int rows, int 
 
 template <int DQK, int DV, int EMU, bool CLAIMED>
 static cudaError_t launch_fwd_impl_sched(const CUtensorMap& tq, const CUtensorMap& tk,
-                                   const CUtensorMap& tv, const FwdParams& p, dim3 grid,
-                                   cudaStream_t stream) {
+                                         const CUtensorMap& tv, const CUtensorMap& to,
+                                         const FwdParams& p, dim3 grid, cudaStream_t stream) {
   using Cfg = FwdCfg<DQK, DV>;
   auto kern = attn_fwd_kernel<DQK, DV, EMU, CLAIMED>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg::kSmemBytes);
+  constexpr int kSmem = (Cfg::kTmaEpi && (DQK == 64 || CLAIMED)) ? Cfg::kSmemBytesEpi : Cfg::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   static_assert(sizeof(FwdBars) <= 512, "barrier block overflows its reservation");
   const int slot = prof_begin(kKFwd, stream);
-  kern<<<grid, 384, Cfg::kSmemBytes, stream>>>(tq, tk, tv, p);
+  kern<<<grid, 384, kSmem, stream>>>(tq, tk, tv, to, p);
   e = cudaGetLastError();
   prof_end(slot, stream);
   return e;
@@ -990,10 +1037,11 @@ static cudaError_t launch_fwd_impl_sched(const CUtensorMap& tq, const CUtensorMa
 // A claimed schedule (tile_ctr set) runs the instance with the scheduler warp.
 template <int DQK, int DV, int EMU>
 static cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk,
-                                   const CUtensorMap& tv, const FwdParams& p, dim3 grid,
-                                   cudaStream_t stream) {
-  if (p.tile_ctr != nullptr) return launch_fwd_impl_sched<DQK, DV, EMU, true>(tq, tk, tv, p, grid, stream);
-  return launch_fwd_impl_sched<DQK, DV, EMU, false>(tq, tk, tv, p, grid, stream);
+                                   const CUtensorMap& tv, const CUtensorMap& to,
+                                   const FwdParams& p, dim3 grid, cudaStream_t stream) {
+  if (p.tile_ctr != nullptr)
+    return launch_fwd_impl_sched<DQK, DV, EMU, true>(tq, tk, tv, to, p, grid, stream);
+  return launch_fwd_impl_sched<DQK, DV, EMU, false>(tq, tk, tv, to, p, grid, stream);
 }
 
 // Number of exponentials per 8 pairs routed to the FMA polynomial (d = 64 has
@@ -1006,13 +1054,15 @@ static cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk,
 #endif
 
 // Supported (d_qk, d_v): (64, 64), (128, 128), (192, 128); the caller checks.
+// `to` maps O like `tq` maps Q (d_v columns, 128 x 64 boxes, 128-byte swizzle).
 cudaError_t launch_attn_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const FwdParams& p, dim3 grid,
-                            cudaStream_t stream) {
-  if (d_qk == 64 && d_v == 64) return launch_fwd_impl<64, 64, ATTN_FWD_EMU_64>(tq, tk, tv, p, grid, stream);
+                            const CUtensorMap& tv, const CUtensorMap& to, const FwdParams& p,
+                            dim3 grid, cudaStream_t stream) {
+  if (d_qk == 64 && d_v == 64)
+    return launch_fwd_impl<64, 64, ATTN_FWD_EMU_64>(tq, tk, tv, to, p, grid, stream);
   if (d_qk == 192 && d_v == 128)
-    return launch_fwd_impl<192, 128, ATTN_FWD_EMU>(tq, tk, tv, p, grid, stream);
-  return launch_fwd_impl<128, 128, ATTN_FWD_EMU>(tq, tk, tv, p, grid, stream);
+    return launch_fwd_impl<192, 128, ATTN_FWD_EMU>(tq, tk, tv, to, p, grid, stream);
+  return launch_fwd_impl<128, 128, ATTN_FWD_EMU>(tq, tk, tv, to, p, grid, stream);
 }
 
 // Largest packed batch the plan kernel sorts (its lengths and order sit in
