@@ -773,7 +773,7 @@ int attn_bwd_dims(const void* q, const void* k, const void* v, const void* o, co
   // q, k (d_qk), v, dO (d_v) with 128-row boxes, the fp32 dQ accumulator
   // (d_qk; 128-row boxes, 64 on CTA pairs), and on CTA pairs q and dO with
   // 64-row boxes
-  CUtensorMap maps[7];
+  CUtensorMap maps[9];
   if (encode_rows_map(&maps[0], q, d_qk, H_q, s.q_rows, s.q_batch) != ATTN_OK ||
       encode_rows_map(&maps[1], k, d_qk, H_kv, s.k_rows, s.q_batch) != ATTN_OK ||
       encode_rows_map(&maps[2], v, d_v, H_kv, s.k_rows, s.q_batch) != ATTN_OK ||
@@ -783,6 +783,10 @@ int attn_bwd_dims(const void* q, const void* k, const void* v, const void* o, co
     return ATTN_ERR_CUDA;
   if (pairs && (encode_rows_map(&maps[5], q, d_qk, H_q, s.q_rows, s.q_batch, false, 64u) != ATTN_OK ||
                 encode_rows_map(&maps[6], dout, d_v, H_q, s.q_rows, s.q_batch, false, 64u) != ATTN_OK))
+    return ATTN_ERR_CUDA;
+  // dK and dV, written by TMA stores from the one-CTA kernel's epilogue
+  if (encode_rows_map(&maps[7], dk, d_qk, H_kv, s.k_rows, s.q_batch) != ATTN_OK ||
+      encode_rows_map(&maps[8], dv, d_v, H_kv, s.k_rows, s.q_batch) != ATTN_OK)
     return ATTN_ERR_CUDA;
 
   BwdParams p;

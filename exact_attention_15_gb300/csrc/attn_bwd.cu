@@ -278,7 +278,8 @@ template <int DQK, int DV, int C0, int NC, bool SPT>
 __global__ void __launch_bounds__(512, 1)
 attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                     const __grid_constant__ CUtensorMap tm_dq, const BwdParams p, int* ticket) {
+                     const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                     const __grid_constant__ CUtensorMap tm_dv, const BwdParams p, int* ticket) {
   using Cfg = BwdCfg<DQK, DV, NC>;
   constexpr bool kDoDV = C0 == 0;          // this pass also accumulates dV
   constexpr int kQS = Cfg::kQStages;
@@ -623,39 +624,72 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       tc_fence_after();
     }
     {
-      // every lane takes part in the (warp-collective) TMEM loads; only rows
-      // inside the sequence are stored
+      // every lane takes part in the (warp-collective) TMEM loads. A whole key
+      // tile leaves through shared memory (the Q stages hold dK, the dS buffer
+      // dV: every MMA is done) and TMA stores of 128 x 64 boxes; the last tile
+      // of a packed sequence row by row, only rows inside the sequence (a
+      // 128-row box would also write the next sequence's rows)
+      const bool tma_epi = !(p.cu_seqlens != nullptr && (t.j + 1) * kTileN > t.Lk);
       const size_t grow = static_cast<size_t>(t.row_base) + kv;
       const size_t krow = p.cu_seqlens ? grow * p.H_kv + t.h_kv
                                        : (static_cast<size_t>(t.b) * p.N_k + kv) * p.H_kv + t.h_kv;
       uint4* dk_row = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dk) + krow * DQK + C0);
       uint4* dv_row = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dv) + krow * DV);
+      uint8_t* const stage_dk = smem + Cfg::kQOff;
+      uint8_t* const stage_dv = smem + Cfg::kdSOff;
 #pragma unroll
       for (int which = kDoDV ? 0 : 1; which < 2; ++which) {
         const uint32_t col = which ? Cfg::kColDK : Cfg::kColDV;
         const float mul = which ? p.scale : 1.0f;
         uint4* dst = which ? dk_row : dv_row;
+        uint8_t* stg = which ? stage_dk : stage_dv;
+        constexpr int kHalfMax = (NC > DV ? NC : DV) / 2;
         const int half = which ? NC / 2 : DV / 2;
+        uint32_t v[kHalfMax];
+        if (have) {
 #pragma unroll
-        for (int cc = 0; cc < half / 32; ++cc) {
-          const int c0 = c * half + cc * 32;
-          uint32_t v[32];
-          if (have) {
-            tmem_ld32(tmem + lane_base + col + c0, v);
-            tmem_ld_wait(v);
-          } else {
+          for (int cc = 0; cc < kHalfMax / 32; ++cc)
+            if (cc < half / 32)
+              tmem_ld32(tmem + lane_base + col + c * half + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(v + cc * 32));
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = 0u;
+          for (int cc = 0; cc < kHalfMax / 32; ++cc)
+            if (cc < half / 32) tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(v + cc * 32));
+        } else {
+#pragma unroll
+          for (int e = 0; e < kHalfMax; ++e) v[e] = 0u;
+        }
+#pragma unroll
+        for (int e = 0; e < kHalfMax / 8; ++e) {
+          if (e >= half / 8) continue;
+          const uint4 w = make_uint4(
+              pack_bf16x2(__uint_as_float(v[8 * e + 0]) * mul, __uint_as_float(v[8 * e + 1]) * mul),
+              pack_bf16x2(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul),
+              pack_bf16x2(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul),
+              pack_bf16x2(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul));
+          const int c8 = c * half + 8 * e;  // first column of these eight in the pass's columns
+          if (tma_epi)
+            *reinterpret_cast<uint4*>(stg + (c8 >> 6) * 16384 + sw128_offset(r, (c8 & 63) >> 3)) = w;
+          else if (kv_ok)
+            dst[c8 / 8] = w;
+        }
+      }
+      if (tma_epi) {
+        fence_async_shared();
+        named_bar_sync(2, 256);  // both compute warpgroups' rows are in place
+        if (c == 0 && r == 0) {
+          const int row = t.row_base + t.j * kTileN;
+#pragma unroll
+          for (int b = 0; b < NC / 64; ++b)
+            tma_store_4d(&tm_dk, smem_addr(stage_dk + b * 16384), C0 + b * 64, t.h_kv, row,
+                         t.batch_coord);
+          if constexpr (kDoDV) {
+#pragma unroll
+            for (int b = 0; b < DV / 64; ++b)
+              tma_store_4d(&tm_dv, smem_addr(stage_dv + b * 16384), b * 64, t.h_kv, row,
+                           t.batch_coord);
           }
-          if (kv_ok) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              dst[c0 / 8 + e] = make_uint4(
-                  pack_bf16x2(__uint_as_float(v[8 * e + 0]) * mul, __uint_as_float(v[8 * e + 1]) * mul),
-                  pack_bf16x2(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul),
-                  pack_bf16x2(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul),
-                  pack_bf16x2(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul));
-          }
+          bulk_commit_group();
+          bulk_wait_group<0>();  // read and written before the CTA's shared memory goes
         }
       }
     }
@@ -766,7 +800,8 @@ static cudaError_t launch_bwd_main(const BwdParams& p, const CUtensorMap* maps, 
                                        Cfg::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int slot = prof_begin(prof_id, st);
-  kern<<<n_work, 512, Cfg::kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p, ticket);
+  kern<<<n_work, 512, Cfg::kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[7],
+                                              maps[8], p, ticket);
   e = cudaGetLastError();
   prof_end(slot, st);
   return e;
