@@ -320,6 +320,34 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     mbar_init(smem_addr(&bars->dq_full), 1);
     mbar_init(smem_addr(&bars->dq_free), 128);
     fence_barrier_init();
+    fence_async_shared();
+    if (n_it > 0) {
+      // K_j, V_j and the first tile's Q and dO go out now (this thread is the
+      // producer's lane 0), so their latency overlaps the rest of the set-up
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      const int row_k = t.row_base + t.j * kTileN;
+      const uint32_t kvb = smem_addr(&bars->kv_full);
+      mbar_arrive_expect_tx(kvb, Cfg::kQKBytes + Cfg::kVBytes);
+      for (int hf = 0; hf < DQK / 64; ++hf)
+        tma_load_4d(smem_addr(smem + Cfg::kKOff) + hf * 16384, &tm_k, kvb, hf * 64, t.h_kv, row_k,
+                    t.batch_coord);
+      for (int hf = 0; hf < DV / 64; ++hf)
+        tma_load_4d(smem_addr(smem + Cfg::kVOff) + hf * 16384, &tm_v, kvb, hf * 64, t.h_kv, row_k,
+                    t.batch_coord);
+      const int h0 = t.h_kv * p.group;
+      const int row_q = t.row_base + bwd_query_tile<SPT>(p, t, 0) * kTileM;
+      const uint32_t fb = smem_addr(&bars->q_full[0]);
+      mbar_expect_tx(fb, Cfg::kQKBytes);
+      for (int hf = 0; hf < DQK / 64; ++hf)
+        tma_load_4d(smem_addr(smem + Cfg::kQOff) + hf * 16384, &tm_q, fb, hf * 64, h0, row_q,
+                    t.batch_coord);
+      const uint32_t db = smem_addr(&bars->do_full);
+      mbar_arrive_expect_tx(db, Cfg::kVBytes);
+      for (int hf = 0; hf < DV / 64; ++hf)
+        tma_load_4d(smem_addr(smem + Cfg::kdOOff) + hf * 16384, &tm_do, db, hf * 64, h0, row_q,
+                    t.batch_coord);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(&bars->tmem_base), Cfg::kTmemCols);
@@ -337,18 +365,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     if (warp == 0) {
       // ------------------------------------------------------- producer
       if (n_it > 0) {
-        if (lane == 0) {
-          tma_prefetch_desc(&tm_q);
-          tma_prefetch_desc(&tm_do);
-          const uint32_t kvb = smem_addr(&bars->kv_full);
-          mbar_arrive_expect_tx(kvb, Cfg::kQKBytes + Cfg::kVBytes);
-          for (int hf = 0; hf < DQK / 64; ++hf)
-            tma_load_4d(smem_addr(smem + Cfg::kKOff) + hf * 16384, &tm_k, kvb, hf * 64, t.h_kv,
-                        t.row_base + t.j * kTileN, t.batch_coord);
-          for (int hf = 0; hf < DV / 64; ++hf)
-            tma_load_4d(smem_addr(smem + Cfg::kVOff) + hf * 16384, &tm_v, kvb, hf * 64, t.h_kv,
-                        t.row_base + t.j * kTileN, t.batch_coord);
-        }
+        // (K_j, V_j and tile 0's Q and dO were issued during the set-up)
         float* stat = reinterpret_cast<float*>(smem + Cfg::kStatOff);
         // LSE (to log2 units) and D of the 128 rows of a query tile, four rows a
         // lane; rows past the end get LSE = +inf so that their P is exactly 0.
@@ -383,7 +400,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             break;
           }
           const uint32_t fb = smem_addr(&bars->q_full[stage]);
-          if (lane == 0) {
+          if (lane == 0 && it > 0) {
             mbar_expect_tx(fb, Cfg::kQKBytes);
             for (int hf = 0; hf < DQK / 64; ++hf)
               tma_load_4d(smem_addr(smem + Cfg::kQOff + stage * Cfg::kQKBytes) + hf * 16384, &tm_q,
@@ -405,7 +422,7 @@ attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             record_error(p.err, kErrTimeout);
             break;
           }
-          if (lane == 0) {
+          if (lane == 0 && it > 0) {
             const uint32_t db = smem_addr(&bars->do_full);
             mbar_arrive_expect_tx(db, Cfg::kVBytes);
             for (int hf = 0; hf < DV / 64; ++hf)
